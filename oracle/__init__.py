@@ -1,0 +1,9 @@
+"""ORACLE -- test infrastructure, not part of the product.
+
+A plain CPU reference of the SVDQuant W4A4 linear operator in fp64
+("SVDQuant W4A4 on Blackwell" §2, §3.1).  Only tests/, the package's smoke
+check and bench.py's CPU-baseline leg may import it.
+"""
+
+from .svdq_ref import (bf16_value, build, e2m1, e4m3, forward, num_threads,  # noqa: F401
+                       round_bf16_bits)
