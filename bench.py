@@ -1,0 +1,360 @@
+"""Throughput of the W4A4 NVFP4 + LoRA linear operator on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step is one operator call (the whole path: scale relayout, LoRA operand
+prep, LoRA + block-scaled MMAs, fused affine epilogue) over one synthetic
+input batch.  The default workload is the 4096 x 3072 x 3072, R=32
+attention-projection shape.  Prints one JSON line (rank 0).
+
+TFLOPS counts 2MNK + 2MNR.  Device time comes from CUDA events around each
+launch on the launching stream, with L2 flushed (a 256 MiB memset, outside
+the events) before every timed launch.  `e2e` times the same call through
+the public API with the inputs copied from pinned host memory and the
+result copied back inside the timed region.  `--impl reference` times the
+CPU oracle on bounded row samples of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25      # dense fp4 / bf16 tensor throughput, nominal
+FALLBACK_BF16_TFLOPS = 1900.0
+BASELINE_PEAK_TFLOPS = 10000.0           # the dense NVFP4 peak the metric is quoted against
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="attn_proj_4096x3072x3072_r32")
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("nvfp4_w4a4_quantized_gb300/csrc/svdq_kernel.cuh",
+                "nvfp4_w4a4_quantized_gb300/csrc/ptx.cuh",
+                "nvfp4_w4a4_quantized_gb300/csrc/svdq_api.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        ent = rec.get(workload)
+        if ent and ent.get("kernel_source_hash") == kernel_source_hash():
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"svdq_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        try:
+            rows = [ln.split(",") for ln in open(self.path).read().strip().splitlines()]
+        except Exception:
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 7:
+                continue
+            try:
+                sm.append(float(r[0]))
+                mx = max(mx, float(r[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(w, inp, target_s=12.0, max_rows=None):
+    """Time the oracle on a bounded row sample; returns (tflops, rows, seconds, threads)."""
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    rows_all = np.arange(w.M, dtype=np.int64)
+    n = 8
+    t = 0.0
+    while True:
+        rows = rows_all[:n]
+        t0 = time.perf_counter()
+        oracle.forward(inp, w.M, w.N, w.K, w.R, rows=rows)
+        t = time.perf_counter() - t0
+        if t >= target_s or n >= (max_rows or w.M):
+            break
+        n = min(max_rows or w.M, max(n + 1, int(n * min(8.0, 1.2 * target_s / max(t, 1e-3)))))
+    flops = 2.0 * n * w.N * (w.K + w.R)
+    return flops / t / 1e12, n, t, oracle.num_threads()
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    from nvfp4_w4a4_quantized_gb300 import synth
+
+    inp = synth.make_workload_inputs(w)
+    per_step_target = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    _, rows, _, threads = oracle_sample(w, inp, target_s=per_step_target)
+    import numpy as np
+
+    import oracle
+
+    sel = np.arange(rows, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle.forward(inp, w.M, w.N, w.K, w.R, rows=sel[: max(1, rows // 4)])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(inp, w.M, w.N, w.K, w.R, rows=sel)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    flops = 2.0 * rows * w.N * (w.K + w.R)
+    val = flops / t / 1e12
+    line = {
+        "impl": "reference", "metric": "W4A4+LoRA GEMM TFLOPS (2MNK+2MNR)", "value": val,
+        "unit": "TFLOPS", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "R": w.R,
+                   "parallelism": "single process, OpenMP over output rows"},
+        "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"first {rows} of {w.M} output rows per step (all N columns)"},
+        "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+
+    import nvfp4_w4a4_quantized_gb300 as pkg
+    from nvfp4_w4a4_quantized_gb300 import build, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    build.build()
+    pkg.load()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    inp = synth.make_workload_inputs(w)
+    d = {k: v.to(dev) for k, v in inp.items()}
+    out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+    opts = dict(tile_n=args.tile_n, stages=args.stages)
+    plan = pkg.svdq_query_plan(w.M, w.N, w.K, w.R, options=opts)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(o=out, dd=d):
+        pkg.svdq_w4a4_gemm(dd["act"], dd["wgt"], dd["ascales"], dd["wscales"], dd["lora_act_in"],
+                           dd["lora_up"], dd["wcscale"], dd["bias"], o, stream=stream,
+                           options=opts)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    code, site, _ = pkg.svdq_read_device_status(clear=True)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at wait site {site} during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        t_wall = time.perf_counter() - t_wall0
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_mean = statistics.mean(ms)
+    if dist is not None:
+        tt = torch.tensor([ms_mean], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_mean = float(tt.item())
+    code, site, _ = pkg.svdq_read_device_status(clear=True)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at wait site {site} in the timed region")
+
+    # end to end through the public call: pinned host inputs -> device -> op -> host
+    host = {k: v.pin_memory() for k, v in inp.items()}
+    host_out = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    dd = {k: torch.empty_like(v, device=dev) for k, v in inp.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e_ms = []
+    for i in range(args.e2e_steps + 2):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for k in host:
+            dd[k].copy_(host[k], non_blocking=True)
+        step(out, dd)
+        host_out.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        if i >= 2:
+            e_ms.append((time.perf_counter() - t0) * 1e3)
+    e_ms_mean = statistics.mean(e_ms)
+    if dist is not None:
+        tt = torch.tensor([e_ms_mean], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e_ms_mean = float(tt.item())
+
+    flops = float(w.flops)
+    tflops_kernel = flops / (ms_mean * 1e-3) / 1e12
+    value = world * tflops_kernel
+    e2e_value = world * flops / (e_ms_mean * 1e-3) / 1e12
+    bf16_peak, peak_src = load_peaks()
+    fp4_peak = bf16_peak * NOMINAL_FP4_OVER_BF16
+    traffic = committed_traffic(w.name)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, rows, secs, threads = oracle_sample(w, inp, target_s=12.0)
+        cpu = {"value": v, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+               "sample": f"first {rows} of {w.M} output rows, all {w.N} columns "
+                         f"({secs:.1f} s, fp64, OpenMP over rows)"}
+
+    if rank == 0:
+        line = {
+            "metric": "W4A4+LoRA GEMM TFLOPS (2MNK+2MNR)",
+            "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_mean, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "R": w.R,
+                       "l2": "flushed: 256 MiB memset before every timed launch",
+                       "parallelism": f"replicas x{world} (independent problems, no collective)",
+                       "tile": [plan["tile_m"], plan["tile_n"]], "stages": plan["num_ab_stage"],
+                       "grid": plan["grid"]},
+            "mfu_vs_10pf": tflops_kernel / BASELINE_PEAK_TFLOPS,
+            "ms_per_step_min": min(ms), "ms_per_step_median": statistics.median(ms),
+            "wall_s_timed_region": t_wall,
+            "roofline": {"bound": "tensor", "achieved": tflops_kernel, "peak": fp4_peak,
+                         "unit": "TFLOP/s", "frac": tflops_kernel / fp4_peak,
+                         "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16 burst {bf16_peak:.1f} TFLOP/s x nominal "
+                                        f"fp4/bf16 ratio {NOMINAL_FP4_OVER_BF16:g}"},
+            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e_ms_mean},
+            "gpu_launches": args.steps,
+            "cpu_baseline": cpu,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus else 1)))
+    if "WORLD_SIZE" not in os.environ:
+        world = 1
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    from nvfp4_w4a4_quantized_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+    else:
+        run_ours(args, w, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

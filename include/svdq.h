@@ -1,0 +1,161 @@
+/*
+ * svdq.h -- C ABI of the GB300 (sm_103a) SVDQuant W4A4 linear-layer operator.
+ *
+ *     y = scaled_mma(act4, wgt4) * wcscale + bias + lora_act_in @ lora_up
+ *
+ * The operator, its tensors and their dtypes are those of "SVDQuant W4A4 on
+ * Blackwell" §2; the NVFP4 format (two E2M1 nibbles per byte, one FP8-E4M3
+ * scale per 16 K elements, single-level scaling) is §3.1 of the same page.
+ * The calling convention (argument order, NULL meanings, status codes) is
+ * this library's own: the page defines no ABI.
+ *
+ * All functions are plain C.  Pointers named "device" are CUDA device
+ * pointers owned by the caller; the library never frees or retains them.
+ * Nothing in this header uses torch or any C++ type.
+ */
+#ifndef SVDQ_H
+#define SVDQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  Every entry point returns one of these synchronously; an
+ * execution fault inside the kernel surfaces, as usual with CUDA, at the
+ * caller's next synchronising call. */
+#define SVDQ_OK 0
+#define SVDQ_ERR_INVALID_ARG -1        /* NULL required pointer, negative size, K == 0 */
+#define SVDQ_ERR_UNSUPPORTED_SHAPE -2  /* M,N not multiples of 16, K not a multiple of 64,
+                                          R > 128, or a size beyond the limits below   */
+#define SVDQ_ERR_MISALIGNED -3         /* a tensor pointer not 16-byte aligned          */
+#define SVDQ_ERR_UNSUPPORTED_DEVICE -4 /* current device is not compute capability 10.3 */
+#define SVDQ_ERR_LAUNCH -5             /* the kernel launch was rejected                */
+#define SVDQ_ERR_CUDA -6               /* another CUDA runtime/driver call failed       */
+#define SVDQ_ERR_TIMEOUT -7            /* device status only: a bounded wait expired     */
+#define SVDQ_ERR_BAD_OPTION -8         /* an svdq_options_t field is out of range       */
+
+/* Size limits: M, N <= 2^24 and K <= 2^20 (elements). */
+#define SVDQ_MAX_MN (1LL << 24)
+#define SVDQ_MAX_K (1LL << 20)
+#define SVDQ_MAX_RANK 128
+
+/*
+ * svdq_w4a4_gemm -- y = scaled_mma(act4, wgt4) * wcscale + bias + lora_act_in @ lora_up
+ * ("SVDQuant W4A4 on Blackwell" §2, §3.1, and the fused epilogue of §6.6).
+ *
+ * act         device, uint8 [M, K/2] row-major: element (m, k) is the E2M1 code
+ *             in the low nibble of byte act[m][k/2] for even k, the high nibble
+ *             for odd k.
+ * wgt         device, uint8 [N, K/2], same packing (K-major; y uses act . wgt^T).
+ * ascales     device, uint8 [K/16, M] FP8-E4M3, M contiguous: ascales[g][m]
+ *             scales act[m][16g .. 16g+15].  Scales must be finite and
+ *             non-negative (the tensor core reads them as unsigned E4M3).
+ * wscales     device, uint8 [K/16, N] FP8-E4M3, likewise for wgt.
+ * lora_act_in device, fp32 [M, R] row-major; NULL if and only if R == 0.
+ * lora_up     device, bf16 [N, R] row-major; NULL if and only if R == 0.
+ * wcscale     device, bf16 [N]; NULL means 1.  With R > 0 every wcscale[n]
+ *             must be finite and non-zero (the LoRA operand is pre-divided
+ *             by it so that LoRA and the main product share one accumulator);
+ *             a zero wcscale[n] drops the LoRA term of column n.
+ * bias        device, bf16 [N]; NULL means 0.
+ * out         device, bf16 [M, N] row-major; every element is written.
+ * M, N        multiples of 16 (the scale tensors' rows must be 16-byte
+ *             strided); M == 0 or N == 0 is an empty product and returns
+ *             SVDQ_OK without launching.
+ * K           a positive multiple of 64.
+ * R           LoRA rank, 0 <= R <= 128 (any value; padded internally).
+ * stream      a cudaStream_t (0 = the legacy default stream).
+ *
+ * Every pointer must be 16-byte aligned.
+ *
+ * The computation is asynchronous on `stream`; the call never synchronises
+ * and allocates no device memory.  Inputs must not be modified and `out`
+ * must not be read until the stream reaches the call.  `out` must not
+ * overlap any input.  Accumulation is fp32 in tensor memory; the result is
+ * rounded to bf16 once.  The call is thread-safe; concurrent calls on
+ * different streams are independent.
+ */
+int svdq_w4a4_gemm(const void* act, const void* wgt, const void* ascales, const void* wscales,
+                   const float* lora_act_in, const void* lora_up, const void* wcscale,
+                   const void* bias, void* out, int64_t M, int64_t N, int64_t K, int64_t R,
+                   void* stream);
+
+/* Optional knobs.  Zero-initialise and set only what is needed; a NULL
+ * options pointer equals all zeros. */
+typedef struct svdq_options {
+    int32_t tile_n;      /* 0 = planner's choice; else 128 or 256                  */
+    int32_t stages;      /* 0 = pipeline-depth solver's choice; else forced (2..8)  */
+    int32_t max_ctas;    /* 0 = one persistent CTA per SM; else cap on the grid    */
+    int32_t timeout_ms;  /* bounded-wait limit inside the kernel; 0 = 2000 ms       */
+    int32_t debug_fault; /* tests only: 1 starts the accumulator producer at the
+                            wrong phase, so the kernel must time out and report
+                            SVDQ_ERR_TIMEOUT instead of hanging                    */
+    int32_t cta_group;   /* 0 = planner's choice; 1 = one CTA per MMA, 2 = a CTA pair
+                            issuing 256-row MMAs (tile_n must then be 256)           */
+    int32_t reserved[2]; /* must be zero                                            */
+} svdq_options_t;
+
+/* svdq_w4a4_gemm with options; identical semantics otherwise. */
+int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* ascales, const void* wscales,
+                      const float* lora_act_in, const void* lora_up, const void* wcscale,
+                      const void* bias, void* out, int64_t M, int64_t N, int64_t K, int64_t R,
+                      const svdq_options_t* options, void* stream);
+
+/* The launch plan the library would use (host only; touches no device when
+ * sm_count > 0).  Shared-memory accounting follows "SVDQuant W4A4 on
+ * Blackwell" §7 (pipeline depth solved from the per-SM budget after every
+ * other buffer; operands split across a CTA pair are counted per CTA). */
+typedef struct svdq_plan {
+    int32_t tile_m, tile_n, tile_k;  /* output tile per cluster and K per ring item  */
+    int32_t cta_group;               /* CTAs sharing one MMA (1 or 2)                */
+    int32_t num_ab_stage;            /* ring depth (K-blocks in flight)              */
+    int32_t num_acc_stage;           /* accumulator buffers in tensor memory         */
+    int32_t stage_bytes;             /* shared-memory bytes per ring stage, per CTA  */
+    int32_t lora_block_bytes;        /* LoRA operand bytes per ring item, per CTA    */
+    int32_t lora_blocks;             /* LoRA ring items per tile (R padded to 64)    */
+    int32_t k_blocks;                /* main ring items per tile                     */
+    int32_t smem_bytes;              /* dynamic shared memory per CTA                */
+    int32_t tmem_cols;               /* tensor-memory columns allocated per CTA      */
+    int32_t tmem_cols_used;          /* of which used                                */
+    int32_t threads;                 /* threads per CTA                              */
+    int64_t num_tiles;               /* output tiles                                 */
+    int32_t grid;                    /* persistent CTAs launched                     */
+    int32_t sm_count;                /* SMs the grid was sized for                   */
+} svdq_plan_t;
+
+/* Fill *plan for the given shape.  sm_count <= 0 queries the current device
+ * (SVDQ_ERR_UNSUPPORTED_DEVICE if none); sm_count > 0 plans for that many
+ * SMs with GB300 limits (227 KB shared memory per block, 512 TMEM columns)
+ * and touches no device. */
+int svdq_query_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* options,
+                    int32_t sm_count, svdq_plan_t* plan);
+
+/* Per-CTA LoRA prologue bytes of one pipeline stage when an A-side operand
+ * [tile_m, R] and a B-side operand [tile_n, R] of elem_bytes each are split
+ * across cta_group CTAs: A along M, B along N, so BOTH are divided by
+ * cta_group ("SVDQuant W4A4 on Blackwell" §7.1-7.5).  Writes the two parts
+ * to *la_bytes / *lu_bytes (either may be NULL) and returns their sum, or a
+ * negative status for bad arguments. */
+int64_t svdq_lora_stage_bytes(int64_t tile_m, int64_t tile_n, int64_t R, int64_t elem_bytes,
+                              int64_t cta_group, int64_t* la_bytes, int64_t* lu_bytes);
+
+/* Read (and if clear != 0, reset) the library's device status word for the
+ * current device: *code is SVDQ_OK or SVDQ_ERR_TIMEOUT, *site identifies
+ * the wait that expired, *block the CTA.  Synchronises the device.  Any of
+ * the output pointers may be NULL. */
+int svdq_read_device_status(int32_t* code, int32_t* site, int32_t* block, int clear);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* svdq_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int svdq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVDQ_H */

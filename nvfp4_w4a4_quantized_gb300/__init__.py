@@ -1,0 +1,13 @@
+"""GB300 (sm_103a) SVDQuant W4A4 linear-layer operator.
+
+    y = scaled_mma(act4, wgt4) * wcscale + bias + lora_act_in @ lora_up
+
+The operator runs in the CUDA library ``libsvdq.so`` (C ABI: include/svdq.h);
+this package holds its build script, a ctypes binding with the same entry
+point names, and the seeded synthetic input generator.
+"""
+
+from .binding import (SVDQ_ERR_BAD_OPTION, SVDQ_ERR_INVALID_ARG, SVDQ_ERR_MISALIGNED,  # noqa: F401
+                      SVDQ_ERR_TIMEOUT, SVDQ_ERR_UNSUPPORTED_DEVICE, SVDQ_ERR_UNSUPPORTED_SHAPE,
+                      SVDQ_OK, SvdqError, SvdqOptions, load, status_string, svdq_lora_stage_bytes,
+                      svdq_query_plan, svdq_read_device_status, svdq_version, svdq_w4a4_gemm)

@@ -1,0 +1,213 @@
+"""ctypes binding of the C ABI in include/svdq.h.
+
+Argument marshalling only: every step of the operator runs in the CUDA
+library.  If ``libsvdq.so`` is missing or fails to load, importing the
+entry points raises -- there is no fallback of any kind.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libsvdq.so")
+
+SVDQ_OK = 0
+SVDQ_ERR_INVALID_ARG = -1
+SVDQ_ERR_UNSUPPORTED_SHAPE = -2
+SVDQ_ERR_MISALIGNED = -3
+SVDQ_ERR_UNSUPPORTED_DEVICE = -4
+SVDQ_ERR_LAUNCH = -5
+SVDQ_ERR_CUDA = -6
+SVDQ_ERR_TIMEOUT = -7
+SVDQ_ERR_BAD_OPTION = -8
+
+# Every symbol include/svdq.h declares.
+EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_query_plan", "svdq_lora_stage_bytes",
+            "svdq_read_device_status", "svdq_status_string", "svdq_version")
+
+
+class SvdqOptions(ctypes.Structure):
+    _fields_ = [("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
+                ("debug_fault", ctypes.c_int32), ("cta_group", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
+
+
+class SvdqPlan(ctypes.Structure):
+    _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32),
+                ("cta_group", ctypes.c_int32), ("num_ab_stage", ctypes.c_int32),
+                ("num_acc_stage", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
+                ("lora_block_bytes", ctypes.c_int32), ("lora_blocks", ctypes.c_int32),
+                ("k_blocks", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("tmem_cols", ctypes.c_int32), ("tmem_cols_used", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("num_tiles", ctypes.c_int64),
+                ("grid", ctypes.c_int32), ("sm_count", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class SvdqError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})" if what else
+                         f"{status_string(status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load libsvdq.so (raises OSError/RuntimeError if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library not built: {p} (run nvfp4_w4a4_quantized_gb300.build)")
+        # the CUDA runtime must be the one torch uses when both are in-process
+        try:
+            import torch  # noqa: F401
+        except ImportError:  # pragma: no cover
+            pass
+        lib = ctypes.CDLL(p, mode=ctypes.RTLD_GLOBAL)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        lib.svdq_w4a4_gemm.restype = ctypes.c_int
+        lib.svdq_w4a4_gemm.argtypes = [vp] * 9 + [i64] * 4 + [vp]
+        lib.svdq_w4a4_gemm_ex.restype = ctypes.c_int
+        lib.svdq_w4a4_gemm_ex.argtypes = [vp] * 9 + [i64] * 4 + [ctypes.POINTER(SvdqOptions), vp]
+        lib.svdq_query_plan.restype = ctypes.c_int
+        lib.svdq_query_plan.argtypes = [i64] * 4 + [ctypes.POINTER(SvdqOptions), i32,
+                                                    ctypes.POINTER(SvdqPlan)]
+        lib.svdq_lora_stage_bytes.restype = i64
+        lib.svdq_lora_stage_bytes.argtypes = [i64] * 5 + [ctypes.POINTER(i64)] * 2
+        lib.svdq_read_device_status.restype = ctypes.c_int
+        lib.svdq_read_device_status.argtypes = [ctypes.POINTER(i32)] * 3 + [ctypes.c_int]
+        lib.svdq_status_string.restype = ctypes.c_char_p
+        lib.svdq_status_string.argtypes = [ctypes.c_int]
+        lib.svdq_version.restype = ctypes.c_int
+        lib.svdq_version.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().svdq_status_string(int(status)).decode()
+
+
+def _opts(options) -> Optional[SvdqOptions]:
+    if options is None:
+        return None
+    if isinstance(options, SvdqOptions):
+        return options
+    o = SvdqOptions()
+    for k, v in dict(options).items():
+        setattr(o, k, int(v))
+    return o
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_handle(stream, device) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def svdq_w4a4_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out,
+                   stream=None, options=None, check: bool = True) -> int:
+    """y = scaled_mma(act4, wgt4) * wcscale + bias + lora_act_in @ lora_up into ``out``.
+
+    Tensors are CUDA torch tensors with the layouts of include/svdq.h
+    (act uint8 [M, K/2], wgt uint8 [N, K/2], ascales uint8 [K/16, M],
+    wscales uint8 [K/16, N], lora_act_in fp32 [M, R], lora_up bf16 [N, R],
+    wcscale/bias bf16 [N] or None, out bf16 [M, N]).  Asynchronous on
+    ``stream`` (default: torch's current stream).  Raises SvdqError on a
+    non-zero status when ``check``; returns the status otherwise.
+    """
+    import torch
+
+    M, kh = act.shape
+    N = wgt.shape[0]
+    K = 2 * kh
+    R = 0 if lora_act_in is None else int(lora_act_in.shape[1])
+    for name, t, dt in (("act", act, torch.uint8), ("wgt", wgt, torch.uint8),
+                        ("ascales", ascales, torch.uint8), ("wscales", wscales, torch.uint8),
+                        ("lora_act_in", lora_act_in, torch.float32),
+                        ("lora_up", lora_up, torch.bfloat16), ("wcscale", wcscale, torch.bfloat16),
+                        ("bias", bias, torch.bfloat16), ("out", out, torch.bfloat16)):
+        if t is None:
+            continue
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous CUDA {dt}, got {t.dtype} "
+                             f"on {t.device} (contiguous={t.is_contiguous()})")
+    if tuple(wgt.shape) != (N, kh) or tuple(ascales.shape) != (K // 16, M) or \
+            tuple(wscales.shape) != (K // 16, N) or tuple(out.shape) != (M, N):
+        raise ValueError("inconsistent operand shapes")
+    if R and (lora_up is None or tuple(lora_up.shape) != (N, R)):
+        raise ValueError("lora_up must be [N, R]")
+    for name, t in (("wcscale", wcscale), ("bias", bias)):
+        if t is not None and tuple(t.shape) != (N,):
+            raise ValueError(f"{name} must be [N]")
+    lib = load()
+    h = _stream_handle(stream, act.device)
+    opts = _opts(options)
+    args = [_ptr(act), _ptr(wgt), _ptr(ascales), _ptr(wscales), _ptr(lora_act_in),
+            _ptr(lora_up), _ptr(wcscale), _ptr(bias), _ptr(out), M, N, K, R]
+    with torch.cuda.device(act.device):
+        if opts is None:
+            rc = lib.svdq_w4a4_gemm(*args, h)
+        else:
+            rc = lib.svdq_w4a4_gemm_ex(*args, ctypes.byref(opts), h)
+    if check and rc != SVDQ_OK:
+        raise SvdqError(rc, "svdq_w4a4_gemm")
+    return rc
+
+
+def svdq_query_plan(M: int, N: int, K: int, R: int, options=None, sm_count: int = 0) -> dict:
+    plan = SvdqPlan()
+    opts = _opts(options)
+    rc = load().svdq_query_plan(M, N, K, R, ctypes.byref(opts) if opts else None, sm_count,
+                                ctypes.byref(plan))
+    if rc != SVDQ_OK:
+        raise SvdqError(rc, "svdq_query_plan")
+    return plan.as_dict()
+
+
+def svdq_lora_stage_bytes(tile_m: int, tile_n: int, R: int, elem_bytes: int, cta_group: int):
+    la, lu = ctypes.c_int64(), ctypes.c_int64()
+    tot = load().svdq_lora_stage_bytes(tile_m, tile_n, R, elem_bytes, cta_group,
+                                       ctypes.byref(la), ctypes.byref(lu))
+    if tot < 0:
+        raise SvdqError(int(tot), "svdq_lora_stage_bytes")
+    return int(tot), int(la.value), int(lu.value)
+
+
+def svdq_read_device_status(clear: bool = True):
+    code, site, block = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    rc = load().svdq_read_device_status(ctypes.byref(code), ctypes.byref(site),
+                                        ctypes.byref(block), 1 if clear else 0)
+    if rc != SVDQ_OK:
+        raise SvdqError(rc, "svdq_read_device_status")
+    return int(code.value), int(site.value), int(block.value)
+
+
+def svdq_version() -> int:
+    return int(load().svdq_version())

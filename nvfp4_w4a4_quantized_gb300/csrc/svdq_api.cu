@@ -1,0 +1,521 @@
+// svdq_api.cu -- the C ABI declared in include/svdq.h: argument validation,
+// the launch planner (tile choice, shared-memory pipeline-depth solver,
+// tensor-memory column budget, persistent grid), TMA tensor-map encoding and
+// the kernel launch.  Host code only touches the device through the CUDA
+// runtime; nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "svdq.h"
+#include "svdq_kernel.cuh"
+
+namespace svdq {
+
+// Device status word: [0] code, [1] wait site, [2] CTA, [3] spare.
+__device__ int g_device_status[4];
+
+namespace {
+
+constexpr int kGb300SmemOptin = 232448;  // 227 KB dynamic shared memory per block
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultTimeoutMs = 2000;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  int sm_count = 0;
+  int smem_optin = 0;
+  int* status = nullptr;
+  bool attr_set[3] = {false, false, false};  // (1,128), (1,256), (2,256)
+  int max_clusters[3] = {0, 0, 0};
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct Plan {
+  int cta_group = 1;
+  int tile_n = 0;
+  int stages = 0;
+  int acc_stages = 0;
+  int stage_bytes = 0;
+  int lora_block_bytes = 0;
+  int lora_blocks = 0;
+  int k_blocks = 0;
+  int r16 = 0;
+  int smem_bytes = 0;
+  int tmem_cols_used = 0;
+  int tiles_m = 0, tiles_n = 0;
+  long long num_tiles = 0;
+  int grid = 0;  // CTAs
+  int sm_count = 0;
+  int group_m = 0;
+};
+
+int validate_options(const svdq_options_t* o) {
+  if (o == nullptr) return SVDQ_OK;
+  if (o->tile_n != 0 && o->tile_n != 128 && o->tile_n != 256) return SVDQ_ERR_BAD_OPTION;
+  if (o->stages != 0 && (o->stages < 2 || o->stages > kMaxStages)) return SVDQ_ERR_BAD_OPTION;
+  if (o->max_ctas < 0 || o->timeout_ms < 0) return SVDQ_ERR_BAD_OPTION;
+  if (o->debug_fault != 0 && o->debug_fault != 1) return SVDQ_ERR_BAD_OPTION;
+  if (o->cta_group < 0 || o->cta_group > 2) return SVDQ_ERR_BAD_OPTION;
+  if (o->cta_group == 2 && o->tile_n == 128) return SVDQ_ERR_BAD_OPTION;
+  for (int r : o->reserved)
+    if (r != 0) return SVDQ_ERR_BAD_OPTION;
+  return SVDQ_OK;
+}
+
+int validate_shape(int64_t M, int64_t N, int64_t K, int64_t R) {
+  if (M < 0 || N < 0 || K <= 0 || R < 0) return SVDQ_ERR_INVALID_ARG;
+  if (M % 16 || N % 16 || K % 64) return SVDQ_ERR_UNSUPPORTED_SHAPE;
+  if (M > SVDQ_MAX_MN || N > SVDQ_MAX_MN || K > SVDQ_MAX_K || R > SVDQ_MAX_RANK)
+    return SVDQ_ERR_UNSUPPORTED_SHAPE;
+  return SVDQ_OK;
+}
+
+// Per-(CTA group, tile) constants the solver needs.
+struct TileInfo {
+  int stage_bytes, acc_cols, sf_cols, acc_stages, fixed_smem, lora_block_bytes;
+};
+
+template <int CG, int BN>
+TileInfo tile_info() {
+  using L = Layout<CG, BN>;
+  // LoRA ring item: LA' [128][32] bf16 + LU' [BN/CG][32] bf16 + raw LA [128][32] fp32
+  // + wcscale; all inside one stage (both operands divided across a pair).
+  return TileInfo{L::kStageBytes, L::kAccCols, L::kSfCols, L::kAccStages, L::smem_bytes(0),
+                  kBM * kLoraRanks * 2 + L::kBNc * kLoraRanks * 2 + kBM * kLoraRanks * 4 +
+                      2 * L::kBNc};
+}
+
+TileInfo tile_info_for(int cg, int bn) {
+  if (cg == 2) return tile_info<2, 256>();
+  return bn == 256 ? tile_info<1, 256>() : tile_info<1, 128>();
+}
+
+// Tile choice: a CTA pair (256 x 256 cluster tile) halves the operand bytes
+// each CTA streams per MMA; small problems that cannot fill the pairs fall
+// back to single-CTA tiles.
+void choose_tile(int64_t M, int64_t N, const svdq_options_t* o, int* cg, int* bn) {
+  int c = (o && o->cta_group) ? o->cta_group : 0;
+  int n = (o && o->tile_n) ? o->tile_n : 0;
+  if (c == 0) c = (n == 128 || M < 256 || N < 256) ? 1 : 2;
+  if (n == 0) n = (c == 2 || N >= 256) ? 256 : 128;
+  *cg = c;
+  *bn = n;
+}
+
+int make_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* o, int sm_count,
+              int smem_optin, int max_clusters, Plan* out) {
+  Plan pl;
+  choose_tile(M, N, o, &pl.cta_group, &pl.tile_n);
+  const TileInfo ti = tile_info_for(pl.cta_group, pl.tile_n);
+  // Pipeline depth: whatever shared memory is left after the epilogue staging,
+  // per-warp wcscale/bias and barriers, capped by the tensor-memory columns
+  // left after the accumulators.  LoRA needs no dedicated buffer: its ring
+  // items reuse main stages.
+  const int by_smem = (smem_optin - ti.fixed_smem) / ti.stage_bytes;
+  const int by_tmem = (kTmemCols - ti.acc_cols) / ti.sf_cols;
+  int max_stages = by_smem < by_tmem ? by_smem : by_tmem;
+  if (max_stages > kMaxStages) max_stages = kMaxStages;
+  if (o && o->stages) {
+    if (o->stages > max_stages) return SVDQ_ERR_BAD_OPTION;
+    pl.stages = o->stages;
+  } else {
+    pl.stages = max_stages;
+  }
+  if (pl.stages < 2) return SVDQ_ERR_UNSUPPORTED_DEVICE;
+  pl.stage_bytes = ti.stage_bytes;
+  pl.acc_stages = ti.acc_stages;
+  pl.smem_bytes = ti.fixed_smem + pl.stages * ti.stage_bytes;
+  pl.tmem_cols_used = ti.acc_cols + pl.stages * ti.sf_cols;
+  pl.lora_block_bytes = ti.lora_block_bytes;
+  pl.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
+  pl.lora_blocks = static_cast<int>((R + kLoraRanks - 1) / kLoraRanks);
+  pl.r16 = static_cast<int>((R + 15) / 16 * 16);
+  const int tm = kBM * pl.cta_group;
+  pl.tiles_m = static_cast<int>((M + tm - 1) / tm);
+  pl.tiles_n = static_cast<int>((N + pl.tile_n - 1) / pl.tile_n);
+  pl.num_tiles = static_cast<long long>(pl.tiles_m) * pl.tiles_n;
+  if (pl.num_tiles >= (1LL << 31)) return SVDQ_ERR_UNSUPPORTED_SHAPE;
+  pl.sm_count = sm_count;
+  long long clusters = sm_count / pl.cta_group;
+  if (max_clusters > 0 && clusters > max_clusters) clusters = max_clusters;
+  if (clusters > pl.num_tiles) clusters = pl.num_tiles;
+  if (o && o->max_ctas > 0 && clusters * pl.cta_group > o->max_ctas)
+    clusters = o->max_ctas / pl.cta_group > 0 ? o->max_ctas / pl.cta_group : 1;
+  pl.grid = static_cast<int>(clusters * pl.cta_group);
+  pl.group_m = pl.tiles_m < 8 ? (pl.tiles_m > 0 ? pl.tiles_m : 1) : 8;
+  *out = pl;
+  return SVDQ_OK;
+}
+
+int probe_device(int* dev_out, DeviceInfo** info_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SVDQ_ERR_UNSUPPORTED_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return SVDQ_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return SVDQ_ERR_UNSUPPORTED_DEVICE;
+    }
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      void* sym = nullptr;
+      if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) {
+        cudaGetLastError();
+        return SVDQ_ERR_CUDA;
+      }
+      d.status = static_cast<int*>(sym);
+      if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+          cudaGetLastError();
+          return SVDQ_ERR_CUDA;
+        }
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+    }
+    d.probed = true;
+  }
+  if (!d.supported) return SVDQ_ERR_UNSUPPORTED_DEVICE;
+  *dev_out = dev;
+  *info_out = &d;
+  return SVDQ_OK;
+}
+
+template <int CG, int BN>
+constexpr int kernel_index() {
+  return CG == 2 ? 2 : (BN == 256 ? 1 : 0);
+}
+
+// Once per device and kernel: opt in to the shared memory and find how many
+// clusters fit at once.
+template <int CG, int BN>
+int ensure_kernel(DeviceInfo* d, int smem_bytes) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  const int idx = kernel_index<CG, BN>();
+  if (!d->attr_set[idx]) {
+    auto k = svdq_w4a4_kernel<CG, BN>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return SVDQ_ERR_CUDA;
+    }
+    d->max_clusters[idx] = d->sm_count / CG;
+    if (CG == 2) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (d->sm_count / 2));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem_bytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n > 0)
+        d->max_clusters[idx] = n;
+      cudaGetLastError();
+    }
+    d->attr_set[idx] = true;
+  }
+  return SVDQ_OK;
+}
+
+int encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+           const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+           CUtensorMapSwizzle swz) {
+  cuuint64_t gd[2] = {dims[0], rank > 1 ? dims[1] : 1};
+  cuuint64_t gs[1] = {rank > 1 ? strides_bytes[0] : 0};
+  cuuint32_t bx[2] = {box[0], rank > 1 ? box[1] : 1};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r =
+      g_encode(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SVDQ_OK : SVDQ_ERR_CUDA;
+}
+
+struct Operands {
+  const void *act, *wgt, *ascales, *wscales, *la, *lu, *wc, *bias;
+  void* out;
+};
+
+template <int CG, int BN>
+int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams& kp, int64_t M,
+           int64_t N, int64_t K, int64_t R, cudaStream_t stream) {
+  using L = Layout<CG, BN>;
+  (void)dinfo;
+  int rc = SVDQ_OK;
+  alignas(64) CUtensorMap tm[8];
+  const uint64_t u = static_cast<uint64_t>(K / 2);
+  {
+    const uint64_t d_act[2] = {u, static_cast<uint64_t>(M)}, s_act[1] = {u};
+    const uint32_t b_act[2] = {128, kBM};
+    if ((rc = encode(&tm[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.act, d_act, s_act, b_act,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
+      return rc;
+    const uint64_t d_wgt[2] = {u, static_cast<uint64_t>(N)};
+    const uint32_t b_wgt[2] = {128, L::kBNc};
+    if ((rc = encode(&tm[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.wgt, d_wgt, s_act, b_wgt,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
+      return rc;
+    const uint64_t d_sfa[2] = {static_cast<uint64_t>(M), static_cast<uint64_t>(K / 16)},
+                   s_sfa[1] = {static_cast<uint64_t>(M)};
+    const uint32_t b_sfa[2] = {kBM, 16};
+    if ((rc = encode(&tm[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.ascales, d_sfa, s_sfa, b_sfa,
+                     CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
+      return rc;
+    const uint64_t d_sfb[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K / 16)},
+                   s_sfb[1] = {static_cast<uint64_t>(N)};
+    const uint32_t b_sfb[2] = {BN, 16};
+    if ((rc = encode(&tm[3], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.wscales, d_sfb, s_sfb, b_sfb,
+                     CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
+      return rc;
+    const uint64_t d_out[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)},
+                   s_out[1] = {static_cast<uint64_t>(N) * 2};
+    const uint32_t b_out[2] = {32, 32};
+    if ((rc = encode(&tm[7], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, op.out, d_out, s_out, b_out,
+                     CU_TENSOR_MAP_SWIZZLE_64B)) != SVDQ_OK)
+      return rc;
+  }
+  if (kp.lora_tma) {
+    const uint64_t d_la[2] = {static_cast<uint64_t>(R), static_cast<uint64_t>(M)},
+                   s_la[1] = {static_cast<uint64_t>(R) * 4};
+    const uint32_t b_la[2] = {kLoraRanks, kBM};
+    if ((rc = encode(&tm[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, op.la, d_la, s_la, b_la,
+                     CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
+      return rc;
+    const uint64_t d_lu[2] = {static_cast<uint64_t>(R), static_cast<uint64_t>(N)},
+                   s_lu[1] = {static_cast<uint64_t>(R) * 2};
+    const uint32_t b_lu[2] = {kLoraRanks, L::kBNc};
+    if ((rc = encode(&tm[5], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, op.lu, d_lu, s_lu, b_lu,
+                     CU_TENSOR_MAP_SWIZZLE_64B)) != SVDQ_OK)
+      return rc;
+  } else {
+    tm[4] = tm[0];  // unused
+    tm[5] = tm[0];
+  }
+  if (op.wc != nullptr) {
+    const uint64_t d_wc[1] = {static_cast<uint64_t>(N)};
+    const uint32_t b_wc[1] = {L::kBNc};
+    if ((rc = encode(&tm[6], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 1, op.wc, d_wc, nullptr, b_wc,
+                     CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
+      return rc;
+  } else {
+    tm[6] = tm[0];  // unused
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CG == 2 ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, svdq_w4a4_kernel<CG, BN>, tm[0], tm[1], tm[2],
+                                           tm[3], tm[4], tm[5], tm[6], tm[7], kp);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return SVDQ_ERR_LAUNCH;
+  }
+  return SVDQ_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace svdq
+
+using namespace svdq;
+
+extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* ascales,
+                                 const void* wscales, const float* lora_act_in,
+                                 const void* lora_up, const void* wcscale, const void* bias,
+                                 void* out, int64_t M, int64_t N, int64_t K, int64_t R,
+                                 const svdq_options_t* options, void* stream) {
+  int rc = validate_options(options);
+  if (rc != SVDQ_OK) return rc;
+  if (!act || !wgt || !ascales || !wscales || !out) return SVDQ_ERR_INVALID_ARG;
+  if (R > 0 && (!lora_act_in || !lora_up)) return SVDQ_ERR_INVALID_ARG;
+  if ((rc = validate_shape(M, N, K, R)) != SVDQ_OK) return rc;
+  const void* ptrs[] = {act, wgt, ascales, wscales, out, lora_act_in, lora_up, wcscale, bias};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return SVDQ_ERR_MISALIGNED;
+  if (M == 0 || N == 0) return SVDQ_OK;
+
+  int dev = 0;
+  DeviceInfo* dinfo = nullptr;
+  if ((rc = probe_device(&dev, &dinfo)) != SVDQ_OK) return rc;
+  Plan pl;
+  {
+    int cg = 1, bn = 256;
+    choose_tile(M, N, options, &cg, &bn);
+    if (cg == 2)
+      rc = ensure_kernel<2, 256>(dinfo, dinfo->smem_optin);
+    else if (bn == 256)
+      rc = ensure_kernel<1, 256>(dinfo, dinfo->smem_optin);
+    else
+      rc = ensure_kernel<1, 128>(dinfo, dinfo->smem_optin);
+    if (rc != SVDQ_OK) return rc;
+    const int idx = cg == 2 ? 2 : (bn == 256 ? 1 : 0);
+    if ((rc = make_plan(M, N, K, R, options, dinfo->sm_count, dinfo->smem_optin,
+                        dinfo->max_clusters[idx], &pl)) != SVDQ_OK)
+      return rc;
+  }
+
+  KParams kp;
+  std::memset(&kp, 0, sizeof kp);
+  kp.M = static_cast<int>(M);
+  kp.N = static_cast<int>(N);
+  kp.K = static_cast<int>(K);
+  kp.R = static_cast<int>(R);
+  kp.tiles_m = pl.tiles_m;
+  kp.tiles_n = pl.tiles_n;
+  kp.num_tiles = static_cast<int>(pl.num_tiles);
+  kp.group_m = pl.group_m;
+  kp.k_blocks = pl.k_blocks;
+  kp.lora_blocks = pl.lora_blocks;
+  kp.r16 = pl.r16;
+  kp.num_stages = pl.stages;
+  kp.lora_tma = (R > 0 && R % 8 == 0);
+  kp.debug_fault = options ? options->debug_fault : 0;
+  const int tmo = (options && options->timeout_ms) ? options->timeout_ms : kDefaultTimeoutMs;
+  kp.timeout_ns = static_cast<unsigned long long>(tmo) * 1000000ull;
+  kp.lora_act_in = R > 0 ? lora_act_in : nullptr;
+  kp.lora_up = R > 0 ? static_cast<const __nv_bfloat16*>(lora_up) : nullptr;
+  kp.wcscale = static_cast<const __nv_bfloat16*>(wcscale);
+  kp.bias = static_cast<const __nv_bfloat16*>(bias);
+  kp.status = dinfo->status;
+
+  const Operands op{act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pl.cta_group == 2) return launch<2, 256>(pl, dinfo, op, kp, M, N, K, R, s);
+  if (pl.tile_n == 256) return launch<1, 256>(pl, dinfo, op, kp, M, N, K, R, s);
+  return launch<1, 128>(pl, dinfo, op, kp, M, N, K, R, s);
+}
+
+extern "C" int svdq_w4a4_gemm(const void* act, const void* wgt, const void* ascales,
+                              const void* wscales, const float* lora_act_in, const void* lora_up,
+                              const void* wcscale, const void* bias, void* out, int64_t M,
+                              int64_t N, int64_t K, int64_t R, void* stream) {
+  return svdq_w4a4_gemm_ex(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out,
+                           M, N, K, R, nullptr, stream);
+}
+
+extern "C" int svdq_query_plan(int64_t M, int64_t N, int64_t K, int64_t R,
+                               const svdq_options_t* options, int32_t sm_count,
+                               svdq_plan_t* plan) {
+  if (plan == nullptr) return SVDQ_ERR_INVALID_ARG;
+  int rc = validate_options(options);
+  if (rc != SVDQ_OK) return rc;
+  if ((rc = validate_shape(M, N, K, R)) != SVDQ_OK) return rc;
+  int smem = kGb300SmemOptin;
+  if (sm_count <= 0) {
+    int dev = 0;
+    DeviceInfo* d = nullptr;
+    if ((rc = probe_device(&dev, &d)) != SVDQ_OK) return rc;
+    sm_count = d->sm_count;
+    smem = d->smem_optin;
+  }
+  Plan pl;
+  if ((rc = make_plan(M, N, K, R, options, sm_count, smem, 0, &pl)) != SVDQ_OK) return rc;
+  std::memset(plan, 0, sizeof *plan);
+  plan->tile_m = kBM * pl.cta_group;
+  plan->tile_n = pl.tile_n;
+  plan->tile_k = kBK;
+  plan->cta_group = pl.cta_group;
+  plan->num_ab_stage = pl.stages;
+  plan->num_acc_stage = pl.acc_stages;
+  plan->stage_bytes = pl.stage_bytes;
+  plan->lora_block_bytes = pl.lora_block_bytes;
+  plan->lora_blocks = pl.lora_blocks;
+  plan->k_blocks = pl.k_blocks;
+  plan->smem_bytes = pl.smem_bytes;
+  plan->tmem_cols = kTmemCols;
+  plan->tmem_cols_used = pl.tmem_cols_used;
+  plan->threads = kThreads;
+  plan->num_tiles = pl.num_tiles;
+  plan->grid = pl.grid;
+  plan->sm_count = sm_count;
+  return SVDQ_OK;
+}
+
+extern "C" int64_t svdq_lora_stage_bytes(int64_t tile_m, int64_t tile_n, int64_t R,
+                                         int64_t elem_bytes, int64_t cta_group, int64_t* la_bytes,
+                                         int64_t* lu_bytes) {
+  if (tile_m <= 0 || tile_n <= 0 || R < 0 || elem_bytes <= 0 || cta_group <= 0 ||
+      tile_m % cta_group || tile_n % cta_group)
+    return SVDQ_ERR_INVALID_ARG;
+  const int64_t la = tile_m * R * elem_bytes / cta_group;  // A side split along M
+  const int64_t lu = tile_n * R * elem_bytes / cta_group;  // B side split along N
+  if (la_bytes) *la_bytes = la;
+  if (lu_bytes) *lu_bytes = lu;
+  return la + lu;
+}
+
+extern "C" int svdq_read_device_status(int32_t* code, int32_t* site, int32_t* block, int clear) {
+  int dev = 0;
+  DeviceInfo* d = nullptr;
+  int rc = probe_device(&dev, &d);
+  if (rc != SVDQ_OK) return rc;
+  int st[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(st, d->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return SVDQ_ERR_CUDA;
+  }
+  if (code) *code = st[0];
+  if (site) *site = st[1];
+  if (block) *block = st[2];
+  if (clear) {
+    const int zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(d->status, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return SVDQ_ERR_CUDA;
+    }
+  }
+  return SVDQ_OK;
+}
+
+extern "C" const char* svdq_status_string(int status) {
+  switch (status) {
+    case SVDQ_OK: return "SVDQ_OK";
+    case SVDQ_ERR_INVALID_ARG: return "SVDQ_ERR_INVALID_ARG";
+    case SVDQ_ERR_UNSUPPORTED_SHAPE: return "SVDQ_ERR_UNSUPPORTED_SHAPE";
+    case SVDQ_ERR_MISALIGNED: return "SVDQ_ERR_MISALIGNED";
+    case SVDQ_ERR_UNSUPPORTED_DEVICE: return "SVDQ_ERR_UNSUPPORTED_DEVICE";
+    case SVDQ_ERR_LAUNCH: return "SVDQ_ERR_LAUNCH";
+    case SVDQ_ERR_CUDA: return "SVDQ_ERR_CUDA";
+    case SVDQ_ERR_TIMEOUT: return "SVDQ_ERR_TIMEOUT";
+    case SVDQ_ERR_BAD_OPTION: return "SVDQ_ERR_BAD_OPTION";
+    default: return "SVDQ_ERR_UNKNOWN";
+  }
+}
+
+extern "C" int svdq_version(void) { return 100; }

@@ -1,0 +1,766 @@
+// svdq_kernel.cuh -- persistent, warp-specialised sm_103a kernel for
+//
+//     y = scaled_mma(act4, wgt4) * wcscale + bias + lora_act_in @ lora_up
+//
+// ("SVDQuant W4A4 on Blackwell" §2 operator, §3.1 NVFP4 block-scaled MMA with
+// scales in tensor memory, §3.2 CTA pair sharing one MMA, §3.5 static
+// persistent tile scheduler, §3.6 / §6 warp specialisation, §6.3 LoRA
+// accumulated into the same tensor-memory accumulator, §6.6 fused per-column
+// affine epilogue).
+//
+// Template parameters: CG = CTAs per MMA (1, or 2 for a CTA pair issuing
+// cta_group::2 MMAs of M = 256), BN = output columns per tile.  Each CTA owns
+// 128 output rows; in a pair the leader (cluster rank 0) issues every MMA,
+// A is split along M and B along N between the two CTAs' shared memory.
+//
+// 12 warps per CTA:
+//   warp 0       TMA producer.  Main ring item (one 256-wide K block): packed
+//                act/wgt tiles (128-byte swizzle) and the raw [16 groups x rows]
+//                scale boxes.  LoRA ring item (32 ranks): raw fp32 LA rows,
+//                bf16 LU rows (64-byte swizzle) and wcscale.
+//   warp 1       MMA issuer (one thread, leader CTA): tcgen05.mma kind::mxf4nvf4
+//                block_scale.scale_vec::4X for main items, kind::f16 (bf16) for
+//                LoRA items, commits that free ring stages / publish accumulators.
+//   warps 2, 3   LoRA operand builders: LA' = bf16(LA) and LU' = bf16(LU / wc)
+//                written into the stage in the MMA's K-major 64-byte-swizzle layout.
+//   warps 4..7   epilogue: tcgen05.ld -> fma(acc, wc, bias) -> bf16 -> shared
+//                staging (64-byte swizzle) -> TMA tile store.
+//   warps 8..11  scale feeders: relayout the stage's raw M-major scale boxes into
+//                row-per-lane words and write them into tensor memory with
+//                tcgen05.st (one warp per 32-lane quadrant), off the MMA pipe.
+// Warp 4+q / 8+q own tensor-memory lanes 32q .. 32q+31.
+//
+// Per output tile the ring carries ceil(R/32) LoRA items, then ceil(K/256)
+// main items; every role walks the same item sequence, so stage index and
+// phase bit survive tile boundaries.  LoRA MMAs run first (the first one
+// overwrites the accumulator); one commit+wait orders them before the
+// block-scaled MMAs of another kind.  LU' is pre-divided by wcscale, so the
+// epilogue's acc * wcscale restores LA @ LU unscaled, as the operator states.
+//
+// Every mbarrier wait is bounded by %globaltimer; on expiry the kernel records
+// SVDQ_ERR_TIMEOUT and the wait site, every role leaves its loop, in-flight
+// TMA and tcgen05 work is drained with a second bounded wait, tensor memory is
+// freed and the CTA exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace svdq {
+
+constexpr int kThreads = 384;
+constexpr int kBM = 128;     // output rows per CTA (per-CTA MMA M)
+constexpr int kBK = 256;     // K elements per main ring item (128 packed bytes per row)
+constexpr int kLoraRanks = 32;  // ranks per LoRA ring item
+constexpr int kMaxStages = 8;
+constexpr int kTmemCols = 512;
+constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;  // teardown drain limit
+
+enum WaitSite : int {
+  kSiteProducerEmpty = 1,
+  kSiteMmaAccEmpty = 2,
+  kSiteMmaFull = 3,
+  kSiteMmaReady = 4,
+  kSiteMmaLoraDone = 5,
+  kSiteLoraAuxFull = 6,
+  kSiteSfAuxFull = 7,
+  kSiteEpiAccFull = 8,
+  kSiteSfTranspose = 9,
+};
+
+constexpr int kStatusTimeout = -7;  // == SVDQ_ERR_TIMEOUT
+
+template <int CG, int BN>
+struct Layout {
+  static_assert(CG == 1 || CG == 2, "CTA group is 1 or 2");
+  static_assert(BN == 128 || BN == 256, "tile_n is 128 or 256");
+  static_assert(!(CG == 2 && BN == 128), "a CTA pair uses 256-wide tiles");
+  static constexpr int kBNc = BN / CG;                // B rows held by this CTA
+  static constexpr int kOffA = 0;                     // 128 rows x 128 B
+  static constexpr int kOffB = kBM * 128;             // kBNc rows x 128 B
+  static constexpr int kOffSFA = kOffB + kBNc * 128;  // raw [16 groups][128 rows]
+  static constexpr int kOffSFB = kOffSFA + 16 * kBM;  // raw [16 groups][BN cols] (whole N tile)
+  static constexpr int kStageBytes = kOffSFB + 16 * BN;
+  static constexpr int kSfbHalves = BN / 128;
+  // LoRA item: LA' [128][32] bf16 and LU' [kBNc][32] bf16 (64-byte rows,
+  // 64-byte swizzle), raw LA [128][32] fp32, wcscale [kBNc] bf16.
+  static constexpr bool kLuInA = kBNc * 64 <= 8192;
+  static constexpr int kLoraLA = kOffA;
+  static constexpr int kLoraLU = kLuInA ? kOffA + 8192 : kOffB;
+  static constexpr int kLoraRawLA = kLuInA ? kOffB : kOffB + kBNc * 64;
+  static constexpr int kLoraWC = kOffSFA;
+  static_assert(kLoraRawLA + kBM * kLoraRanks * 4 <= kOffSFA, "LoRA item fits the stage");
+  static_assert(2 * kBNc <= 16 * kBM, "wcscale fits the scale area");
+  static constexpr int kAccStages = (BN == 256) ? 1 : 2;
+  static constexpr int kAccCols = kAccStages * BN;
+  static constexpr int kSfCols = 16 + 16 * kSfbHalves;  // tensor-memory scale columns per stage
+  static constexpr int kEpiStageBytes = 32 * 64;        // one 32 x 32 bf16 output tile
+  static constexpr int kEpiBytes = 4 * 2 * kEpiStageBytes;
+  static constexpr int kWcbBytes = 4 * 2 * BN * 2;      // per epilogue warp: wc[BN], bias[BN]
+  static constexpr int kBarCount = 5 * kMaxStages + 6;
+  static constexpr int kBarBytes = 8 * kBarCount + 16;
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+  __host__ __device__ static constexpr int epi_offset(int stages) { return stages * kStageBytes; }
+  __host__ __device__ static constexpr int wcb_offset(int stages) {
+    return epi_offset(stages) + kEpiBytes;
+  }
+  __host__ __device__ static constexpr int bars_offset(int stages) {
+    return wcb_offset(stages) + kWcbBytes;
+  }
+  __host__ __device__ static constexpr int smem_bytes(int stages) {
+    return 1024 /* alignment slack */ + bars_offset(stages) + kBarBytes;
+  }
+  __host__ __device__ static constexpr int tmem_cols_used(int stages) {
+    return kAccCols + stages * kSfCols;
+  }
+};
+
+struct KParams {
+  int M, N, K, R;
+  int tiles_m, tiles_n, num_tiles, group_m;
+  int k_blocks;     // ceil(K / 256)
+  int lora_blocks;  // ceil(R / 32)
+  int r16;          // R rounded up to 16
+  int num_stages;
+  int lora_tma;     // R % 8 == 0: LoRA rows arrive by TMA; else direct loads
+  int debug_fault;
+  unsigned long long timeout_ns;
+  const float* lora_act_in;
+  const __nv_bfloat16* lora_up;
+  const __nv_bfloat16* wcscale;
+  const __nv_bfloat16* bias;
+  int* status;
+};
+
+// Grouped raster over cluster tiles: group_m M-blocks sweep all N-blocks.
+__device__ __forceinline__ void tile_coords(const KParams& p, int t, int& mb, int& nb) {
+  const int group = p.group_m * p.tiles_n;
+  const int gid = t / group;
+  const int first_m = gid * p.group_m;
+  const int gsz = min(p.tiles_m - first_m, p.group_m);
+  const int local = t - gid * group;
+  mb = first_m + local % gsz;
+  nb = local / gsz;
+}
+
+struct Ctl {
+  volatile int* abort_flag;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+__device__ __noinline__ void report_timeout(int* status, int site) {
+  if (atomicCAS(status, 0, kStatusTimeout) == 0) {
+    status[1] = site;
+    status[2] = static_cast<int>(blockIdx.x);
+  }
+}
+
+// Bounded wait for the phase with parity `parity` of a local mbarrier.
+// Returns false (and makes every other role of this CTA give up) on expiry or
+// if another role already gave up.
+template <int CG>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int site, const Ctl& c) {
+  auto probe = [&]() {
+    return CG == 2 ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (probe()) return true;
+    if (*c.abort_flag) return false;
+    if (ptx::globaltimer() - t0 > c.timeout_ns) {
+      *c.abort_flag = 1;
+      report_timeout(c.status, site);
+      return false;
+    }
+  }
+}
+
+template <int CG>
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, int site,
+                                              const Ctl& c) {
+  const bool ok = wait_bar<CG>(bar, parity, site, c);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Teardown wait: ignores the abort flag, short fixed limit.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > kDrainNs) return;
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// In-place relayout of one K-step (4 scale groups) of a raw TMA scale box
+// [4 groups][H*128 rows] into H blocks of 32 rows x 16 bytes: word j of row
+// r of block h holds the 4 group scales (byte g = group g) of row 128h+32j+r.
+template <int H>
+__device__ __forceinline__ void sf_relayout(uint8_t* base, int lane) {
+  uint32_t w[H][4];
+#pragma unroll
+  for (int h = 0; h < H; ++h)
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      w[h][g] = *reinterpret_cast<const uint32_t*>(base + g * (H * 128) + h * 128 + 4 * lane);
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < H; ++h) {
+    // 4x4 byte transpose: output i gathers byte i (row 4*lane+i) of groups 0..3.
+    const uint32_t t0 = __byte_perm(w[h][0], w[h][1], 0x5140);
+    const uint32_t t1 = __byte_perm(w[h][0], w[h][1], 0x7362);
+    const uint32_t t2 = __byte_perm(w[h][2], w[h][3], 0x5140);
+    const uint32_t t3 = __byte_perm(w[h][2], w[h][3], 0x7362);
+    uint8_t* dst = base + 512 * h + (lane >> 3) * 4;
+    const int r0 = 4 * (lane & 7);
+    *reinterpret_cast<uint32_t*>(dst + (r0 + 0) * 16) = __byte_perm(t0, t2, 0x5410);
+    *reinterpret_cast<uint32_t*>(dst + (r0 + 1) * 16) = __byte_perm(t0, t2, 0x7632);
+    *reinterpret_cast<uint32_t*>(dst + (r0 + 2) * 16) = __byte_perm(t1, t3, 0x5410);
+    *reinterpret_cast<uint32_t*>(dst + (r0 + 3) * 16) = __byte_perm(t1, t3, 0x7632);
+  }
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..3) of row `row` in a K-major tile
+// with 64-byte rows and the 64-byte swizzle.
+__device__ __forceinline__ int sw64_offset(int row, int chunk) {
+  return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+}
+
+// LA' from the TMA-staged raw fp32 rows [128][32]: lane reads 4 consecutive
+// floats of a row, writes 4 bf16 (half a 16-byte chunk).
+__device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* raw, int lane) {
+  const int c = lane & 7;  // 16-byte piece of the 128-byte raw row
+#pragma unroll 4
+  for (int it = 0; it < kBM / 4; ++it) {
+    const int row = it * 4 + (lane >> 3);
+    const float4 v = *reinterpret_cast<const float4*>(raw + row * 128 + 16 * c);
+    uint2 pk;
+    pk.x = ptx::pack_bf16x2(v.x, v.y);
+    pk.y = ptx::pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2*>(dst + sw64_offset(row, c >> 1) + 8 * (c & 1)) = pk;
+  }
+}
+
+// LU' in place: every 16-byte chunk of row n times 1/wcscale[n] (fp32
+// reciprocal and product, bf16 RNE).  Rows outside N (zero-filled) stay zero.
+template <int ROWS>
+__device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* wc, int n_cta,
+                                                   int N, int lane) {
+  const int pc = lane & 3;
+#pragma unroll 4
+  for (int it = 0; it < ROWS / 8; ++it) {
+    const int row = it * 8 + (lane >> 2);
+    const float w = __uint_as_float(static_cast<uint32_t>(
+                        *reinterpret_cast<const uint16_t*>(wc + 2 * row)) << 16);
+    const float inv = (n_cta + row < N && w != 0.f) ? __frcp_rn(w) : 0.f;
+    uint4 x = *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc);
+    x.x = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.x), inv), __fmul_rn(bf16_hi(x.x), inv));
+    x.y = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.y), inv), __fmul_rn(bf16_hi(x.y), inv));
+    x.z = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.z), inv), __fmul_rn(bf16_hi(x.z), inv));
+    x.w = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.w), inv), __fmul_rn(bf16_hi(x.w), inv));
+    *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc) = x;
+  }
+}
+
+// Direct-load LoRA operands (used when R is not a multiple of 8, so LoRA rows
+// are not 16-byte strided for TMA): LA' rows m_cta.., LU' rows n_cta.., ranks
+// 32*blk .. 32*blk+31, zero outside [M|N, R).
+__device__ __forceinline__ void lora_la_direct(uint8_t* dst, const KParams& p, int m_cta, int blk,
+                                               int lane) {
+  const int chunk = lane & 3;
+  const int r0 = blk * kLoraRanks + chunk * 8;
+  for (int it = 0; it < kBM / 8; ++it) {
+    const int row = it * 8 + (lane >> 2);
+    const int m = m_cta + row;
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      v[q] = (m < p.M && r0 + q < p.R) ? __ldg(p.lora_act_in + (size_t)m * p.R + r0 + q) : 0.f;
+    uint4 pk;
+    pk.x = ptx::pack_bf16x2(v[0], v[1]);
+    pk.y = ptx::pack_bf16x2(v[2], v[3]);
+    pk.z = ptx::pack_bf16x2(v[4], v[5]);
+    pk.w = ptx::pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(dst + sw64_offset(row, chunk)) = pk;
+  }
+}
+
+template <int ROWS>
+__device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p, int n_cta, int blk,
+                                               int lane) {
+  const int chunk = lane & 3;
+  const int r0 = blk * kLoraRanks + chunk * 8;
+  const uint16_t* lu = reinterpret_cast<const uint16_t*>(p.lora_up);
+  const uint16_t* wc = reinterpret_cast<const uint16_t*>(p.wcscale);
+  for (int it = 0; it < ROWS / 8; ++it) {
+    const int row = it * 8 + (lane >> 2);
+    const int n = n_cta + row;
+    float inv = 0.f;
+    if (n < p.N) {
+      const float w = wc ? __uint_as_float(static_cast<uint32_t>(__ldg(wc + n)) << 16) : 1.f;
+      inv = (w != 0.f) ? __frcp_rn(w) : 0.f;
+    }
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      v[q] = (n < p.N && r0 + q < p.R)
+                 ? __fmul_rn(__uint_as_float(static_cast<uint32_t>(
+                                 __ldg(lu + (size_t)n * p.R + r0 + q)) << 16),
+                             inv)
+                 : 0.f;
+    uint4 pk;
+    pk.x = ptx::pack_bf16x2(v[0], v[1]);
+    pk.y = ptx::pack_bf16x2(v[2], v[3]);
+    pk.z = ptx::pack_bf16x2(v[4], v[5]);
+    pk.w = ptx::pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(dst + sw64_offset(row, chunk)) = pk;
+  }
+}
+
+template <int CG, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    svdq_w4a4_kernel(const __grid_constant__ CUtensorMap tm_act,
+                     const __grid_constant__ CUtensorMap tm_wgt,
+                     const __grid_constant__ CUtensorMap tm_sfa,
+                     const __grid_constant__ CUtensorMap tm_sfb,
+                     const __grid_constant__ CUtensorMap tm_la,
+                     const __grid_constant__ CUtensorMap tm_lu,
+                     const __grid_constant__ CUtensorMap tm_wc,
+                     const __grid_constant__ CUtensorMap tm_out, const KParams p) {
+  using L = Layout<CG, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const int warp = static_cast<int>(threadIdx.x) / 32;
+  const int lane = static_cast<int>(threadIdx.x) % 32;
+  const int S = p.num_stages;
+  const int n_items = p.lora_blocks + p.k_blocks;
+  const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+  const bool leader = (rank == 0);
+  const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+  const int num_clusters = static_cast<int>(gridDim.x) / CG;
+
+  uint8_t* bar_area = smem + L::bars_offset(S);
+  const uint32_t bar0 = ptx::smem_u32(bar_area);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+  auto auxfull = [&](int s) { return bar0 + 8u * (2 * kMaxStages + s); };
+  auto ready = [&](int s) { return bar0 + 8u * (3 * kMaxStages + s); };
+  const uint32_t sft = bar0 + 8u * (4 * kMaxStages);
+  auto acc_full = [&](int a) { return bar0 + 8u * (5 * kMaxStages + a); };
+  auto acc_empty = [&](int a) { return bar0 + 8u * (5 * kMaxStages + 2 + a); };
+  const uint32_t lora_done = bar0 + 8u * (5 * kMaxStages + 4);
+  const uint32_t drain = bar0 + 8u * (5 * kMaxStages + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * L::kBarCount);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+  // Barriers the leader owns, addressed from either CTA of the pair.
+  auto to_leader = [&](uint32_t local_bar) {
+    return CG == 2 ? ptx::mapa(local_bar, 0) : local_bar;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(full(s), 1);
+      ptx::mbar_init(empty(s), 1);
+      ptx::mbar_init(auxfull(s), 1);
+      ptx::mbar_init(ready(s), 6 * CG);
+    }
+    ptx::mbar_init(sft, 4);
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(acc_full(a), 1);
+      ptx::mbar_init(acc_empty(a), 4 * CG);
+    }
+    ptx::mbar_init(lora_done, 1);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tm_act);
+    ptx::prefetch_tmap(&tm_wgt);
+    ptx::prefetch_tmap(&tm_sfa);
+    ptx::prefetch_tmap(&tm_sfb);
+  }
+  if (warp == 1) {
+    if (CG == 2) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish();
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (CG == 2) ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      const uint32_t main_aux_bytes = 16 * kBM + 16 * BN;
+      const uint32_t lora_aux_bytes =
+          kBM * kLoraRanks * 4 + L::kBNc * 64 + (p.wcscale != nullptr ? 2 * L::kBNc : 0);
+      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+        int mb, nb;
+        tile_coords(p, t, mb, nb);
+        const int m0 = mb * kBM * CG, n0 = nb * BN;
+        const int m_cta = m0 + kBM * static_cast<int>(rank);
+        const int n_cta = n0 + L::kBNc * static_cast<int>(rank);
+        for (int i = 0; i < n_items; ++i) {
+          if (!wait_bar<CG>(empty(stage), phase ^ 1u, kSiteProducerEmpty, ctl)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + stage * L::kStageBytes;
+          if (i < p.lora_blocks) {
+            if (p.lora_tma) {
+              ptx::mbar_arrive_expect_tx(auxfull(stage), lora_aux_bytes);
+              ptx::tma_load_2d(st + L::kLoraRawLA, &tm_la, auxfull(stage), kLoraRanks * i, m_cta);
+              ptx::tma_load_2d(st + L::kLoraLU, &tm_lu, auxfull(stage), kLoraRanks * i, n_cta);
+              if (p.wcscale != nullptr)
+                ptx::tma_load_1d(st + L::kLoraWC, &tm_wc, auxfull(stage), n_cta);
+            } else {
+              ptx::mbar_arrive(auxfull(stage));
+            }
+            if (leader) ptx::mbar_arrive(full(stage));
+          } else {
+            const int kb = i - p.lora_blocks;
+            ptx::mbar_arrive_expect_tx(auxfull(stage), main_aux_bytes);
+            ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, auxfull(stage), m_cta, kb * 16);
+            ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, auxfull(stage), n0, kb * 16);
+            if (leader) ptx::mbar_arrive_expect_tx(full(stage), CG * (L::kOffSFA - L::kOffA));
+            if (CG == 2) {
+              const uint32_t fb = to_leader(full(stage));
+              ptx::tma_load_2d_pair(st + L::kOffA, &tm_act, fb, kb * 128, m_cta);
+              ptx::tma_load_2d_pair(st + L::kOffB, &tm_wgt, fb, kb * 128, n_cta);
+            } else {
+              ptx::tma_load_2d(st + L::kOffA, &tm_act, full(stage), kb * 128, m_cta);
+              ptx::tma_load_2d(st + L::kOffB, &tm_wgt, full(stage), kb * 128, n_cta);
+            }
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // No TMA write may still be landing in this CTA's shared memory at exit.
+      for (long long j = (issued > S ? issued - S : 0); j < issued; ++j) {
+        const int s = static_cast<int>(j % S);
+        const uint32_t par = static_cast<uint32_t>((j / S) & 1);
+        drain_wait(auxfull(s), par);
+        if (leader) drain_wait(full(s), par);
+      }
+      if (CG == 2 && !leader && !ok) {
+        // The pair's operand loads signal the leader's barriers; after an abort
+        // give any still-landing load a fixed grace period.
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 100000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0, lora_phase = 0;
+      bool ok = true;
+      int tile_iter = 0;
+      constexpr uint32_t kIdescMain = ptx::idesc_mxf4nvf4(kBM * CG, BN);
+      constexpr uint32_t kIdescLora = ptx::idesc_bf16_f32(kBM * CG, BN);
+      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++tile_iter) {
+        const int acc_stage = tile_iter % L::kAccStages;
+        const uint32_t acc_phase = static_cast<uint32_t>(tile_iter / L::kAccStages) & 1u;
+        // A free accumulator: the epilogue released this buffer's previous tile.
+        // (debug_fault inverts the expected phase -- the single-stage
+        // "producer must start at phase 1" mistake -- so the wait expires.)
+        if (!wait_bar<CG>(acc_empty(acc_stage), acc_phase ^ 1u ^ (p.debug_fault ? 1u : 0u),
+                          kSiteMmaAccEmpty, ctl)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc_stage * BN);
+        uint32_t accumulate = 0;
+        for (int i = 0; i < n_items; ++i) {
+          if (!wait_bar<CG>(full(stage), phase, kSiteMmaFull, ctl) ||
+              !wait_bar<CG>(ready(stage), phase, kSiteMmaReady, ctl)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t st = sbase + stage * L::kStageBytes;
+          if (i < p.lora_blocks) {
+            const int nsteps = min(2, (p.r16 - kLoraRanks * i) / 16);
+            for (int s = 0; s < nsteps; ++s) {
+              const uint64_t ad = ptx::desc_kmajor_sw64(st + L::kLoraLA + 32 * s);
+              const uint64_t bd = ptx::desc_kmajor_sw64(st + L::kLoraLU + 32 * s);
+              if (CG == 2)
+                ptx::mma_bf16_pair(d_tmem, ad, bd, kIdescLora, accumulate);
+              else
+                ptx::mma_bf16(d_tmem, ad, bd, kIdescLora, accumulate);
+              accumulate = 1;
+            }
+            if (CG == 2)
+              ptx::mma_commit_pair_multicast(empty(stage), 3);
+            else
+              ptx::mma_commit(empty(stage));
+            if (i == p.lora_blocks - 1) {
+              // Different MMA kinds on one accumulator: let the LoRA products
+              // land before the first block-scaled MMA reads the accumulator.
+              if (CG == 2)
+                ptx::mma_commit_pair(lora_done);
+              else
+                ptx::mma_commit(lora_done);
+              if (!wait_bar<CG>(lora_done, lora_phase, kSiteMmaLoraDone, ctl)) {
+                ok = false;
+                break;
+              }
+              lora_phase ^= 1u;
+              ptx::tc_fence_after();
+            }
+          } else {
+            const int kb = i - p.lora_blocks;
+            const uint32_t sf =
+                tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
+            const int nsteps = min(4, (p.K - kb * kBK) / 64);
+            for (int s = 0; s < nsteps; ++s) {
+              const uint64_t ad = ptx::desc_kmajor_sw128(st + L::kOffA + 32 * s);
+              const uint64_t bd = ptx::desc_kmajor_sw128(st + L::kOffB + 32 * s);
+              const uint32_t sfa = sf + 4 * s, sfb = sf + 16 + 4 * s * L::kSfbHalves;
+              if (CG == 2)
+                ptx::mma_mxf4nvf4_pair(d_tmem, ad, bd, kIdescMain, sfa, sfb, accumulate);
+              else
+                ptx::mma_mxf4nvf4(d_tmem, ad, bd, kIdescMain, sfa, sfb, accumulate);
+              accumulate = 1;
+            }
+            if (CG == 2)
+              ptx::mma_commit_pair_multicast(empty(stage), 3);
+            else
+              ptx::mma_commit(empty(stage));
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (CG == 2)
+          ptx::mma_commit_pair_multicast(acc_full(acc_stage), 3);
+        else
+          ptx::mma_commit(acc_full(acc_stage));
+      }
+      // Every tcgen05 operation issued here completes before tensor memory is freed.
+      if (CG == 2)
+        ptx::mma_commit_pair(drain);
+      else
+        ptx::mma_commit(drain);
+      drain_wait(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ LoRA operand builders
+    int stage = 0;
+    uint32_t phase = 0;
+    const uint32_t ready_bar0 = to_leader(ready(0));
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
+      const int n_cta = nb * BN + L::kBNc * static_cast<int>(rank);
+      bool ok = true;
+      for (int i = 0; i < n_items; ++i) {
+        if (!warp_wait_bar<CG>(auxfull(stage), phase, kSiteLoraAuxFull, ctl)) {
+          ok = false;
+          break;
+        }
+        if (i < p.lora_blocks) {
+          uint8_t* st = smem + stage * L::kStageBytes;
+          if (warp == 2) {
+            if (p.lora_tma)
+              lora_la_from_smem(st + L::kLoraLA, st + L::kLoraRawLA, lane);
+            else
+              lora_la_direct(st + L::kLoraLA, p, m_cta, i, lane);
+          } else {
+            if (!p.lora_tma)
+              lora_lu_direct<L::kBNc>(st + L::kLoraLU, p, n_cta, i, lane);
+            else if (p.wcscale != nullptr)
+              lora_lu_scale_smem<L::kBNc>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, lane);
+          }
+          ptx::fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(ready_bar0 + 8u * stage);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // tensor-memory lane quadrant of this warp
+    const uint16_t* wcg = reinterpret_cast<const uint16_t*>(p.wcscale);
+    const uint16_t* big = reinterpret_cast<const uint16_t*>(p.bias);
+    uint8_t* wcb = smem + L::wcb_offset(S) + q * (4 * BN);  // wc[BN] then bias[BN], bf16
+    uint8_t* stg = smem + L::epi_offset(S) + q * (2 * L::kEpiStageBytes);
+    const uint32_t acc_empty0 = to_leader(acc_empty(0));
+    int tile_iter = 0, buf = 0;
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++tile_iter) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
+      const int n0 = nb * BN;
+      // this tile's wcscale / bias (8 columns per lane) while the accumulator fills
+      uint4 wv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // 1.0
+      uint4 bv = make_uint4(0u, 0u, 0u, 0u);
+      if (lane < BN / 8 && n0 + 8 * lane < p.N) {
+        if (wcg) wv = __ldg(reinterpret_cast<const uint4*>(wcg + n0 + 8 * lane));
+        if (big) bv = __ldg(reinterpret_cast<const uint4*>(big + n0 + 8 * lane));
+      }
+      const int acc_stage = tile_iter % L::kAccStages;
+      const uint32_t acc_phase = static_cast<uint32_t>(tile_iter / L::kAccStages) & 1u;
+      if (!warp_wait_bar<CG>(acc_full(acc_stage), acc_phase, kSiteEpiAccFull, ctl)) break;
+      ptx::tc_fence_after();
+      if (lane < BN / 8) {
+        *reinterpret_cast<uint4*>(wcb + 16 * lane) = wv;
+        *reinterpret_cast<uint4*>(wcb + 2 * BN + 16 * lane) = bv;
+      }
+      __syncwarp();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                             static_cast<uint32_t>(acc_stage * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(taddr + 32 * c, v);
+        ptx::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint4 w8 = lds128(wcb + 2 * (32 * c + 8 * g));
+          const uint4 b8 = lds128(wcb + 2 * BN + 2 * (32 * c + 8 * g));
+          const uint32_t ww[4] = {w8.x, w8.y, w8.z, w8.w};
+          const uint32_t bb[4] = {b8.x, b8.y, b8.z, b8.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float y0 = fmaf(__uint_as_float(v[8 * g + 2 * j]), bf16_lo(ww[j]), bf16_lo(bb[j]));
+            const float y1 =
+                fmaf(__uint_as_float(v[8 * g + 2 * j + 1]), bf16_hi(ww[j]), bf16_hi(bb[j]));
+            pk[4 * g + j] = ptx::pack_bf16x2(y0, y1);
+          }
+        }
+        // staging buffer `buf` must no longer be read by its previous store
+        if (lane == 0) ptx::bulk_wait_group_read<1>();
+        __syncwarp();
+        uint8_t* sb = stg + buf * L::kEpiStageBytes;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(sb + sw64_offset(lane, j)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&tm_out, ptx::smem_u32(sb), n0 + 32 * c, m_cta + 32 * q);
+          ptx::bulk_commit_group();
+        }
+        buf ^= 1;
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(acc_empty0 + 8u * acc_stage);
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ scale feeders
+    const int q = warp & 3;
+    int stage = 0;
+    uint32_t phase = 0, sft_phase = 0;
+    const uint32_t ready_bar0 = to_leader(ready(0));
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+      bool ok = true;
+      for (int i = 0; i < n_items; ++i) {
+        if (!warp_wait_bar<CG>(auxfull(stage), phase, kSiteSfAuxFull, ctl)) {
+          ok = false;
+          break;
+        }
+        if (i >= p.lora_blocks) {
+          uint8_t* st = smem + stage * L::kStageBytes;
+          // this warp relayouts K-step q of the stage; the four warps then share
+          sf_relayout<1>(st + L::kOffSFA + 512 * q, lane);
+          sf_relayout<L::kSfbHalves>(st + L::kOffSFB + 4 * BN * q, lane);
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(sft);
+          if (!warp_wait_bar<CG>(sft, sft_phase, kSiteSfTranspose, ctl)) {
+            ok = false;
+            break;
+          }
+          sft_phase ^= 1u;
+          // row (32q + lane) of tensor memory: words j = rows lane + 32j of
+          // each 128-row block, for K-steps 0..3
+          uint32_t a[16], b[16 * L::kSfbHalves];
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint4 x = lds128(st + L::kOffSFA + 512 * s + 16 * lane);
+            a[4 * s] = x.x; a[4 * s + 1] = x.y; a[4 * s + 2] = x.z; a[4 * s + 3] = x.w;
+#pragma unroll
+            for (int h = 0; h < L::kSfbHalves; ++h) {
+              const uint4 y = lds128(st + L::kOffSFB + 4 * BN * s + 512 * h + 16 * lane);
+              const int o = 4 * (s * L::kSfbHalves + h);
+              b[o] = y.x; b[o + 1] = y.y; b[o + 2] = y.z; b[o + 3] = y.w;
+            }
+          }
+          const uint32_t col = tmem_base + lane_base +
+                               static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
+          ptx::tmem_st_32x32b_x16(col, a);
+#pragma unroll
+          for (int h = 0; h < L::kSfbHalves; ++h) ptx::tmem_st_32x32b_x16(col + 16 + 16 * h, b + 16 * h);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(ready_bar0 + 8u * stage);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (CG == 2) ptx::cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    if (CG == 2)
+      ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace svdq

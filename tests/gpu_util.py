@@ -1,0 +1,66 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the C
+ABI and compare it element by element with the CPU oracle."""
+
+import numpy as np
+import torch
+
+import oracle
+from nvfp4_w4a4_quantized_gb300 import binding
+
+NAN_BF16 = 0x7FC0
+
+
+def to_device(inp, device="cuda"):
+    return {k: (None if v is None else v.to(device)) for k, v in inp.items()}
+
+
+def run_gpu(inp, M, N, K, R, options=None, check_status=True):
+    """Run the CUDA path on `inp` (CPU tensors) and return y as float64 numpy.
+
+    `out` is pre-filled with NaN so an element the kernel fails to write is
+    caught by the finiteness check."""
+    d = to_device(inp)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    la = d["lora_act_in"] if R > 0 else None
+    lu = d["lora_up"] if R > 0 else None
+    binding.svdq_w4a4_gemm(d["act"], d["wgt"], d["ascales"], d["wscales"], la, lu,
+                           d.get("wcscale"), d.get("bias"), out, options=options)
+    torch.cuda.synchronize()
+    if check_status:
+        code, site, block = binding.svdq_read_device_status(clear=True)
+        assert code == 0, f"device status {code} at wait site {site}, CTA {block}"
+    return out.to(torch.float64).cpu().numpy()
+
+
+def parity(y_gpu, y_ref, rel=2.0 ** -7, rms_frac=1e-3, extra=None):
+    """The acceptance bound |y_gpu - y_ref| <= 2^-7 |y_ref| + 1e-3 rms(y_ref),
+    per element (plus an optional per-element allowance).  Returns the worst
+    ratio |delta| / bound (<= 1 passes)."""
+    assert y_gpu.shape == y_ref.shape
+    assert np.all(np.isfinite(y_gpu)), "non-finite output (unwritten element?)"
+    rms = float(np.sqrt(np.mean(y_ref ** 2))) if y_ref.size else 0.0
+    bound = rel * np.abs(y_ref) + rms_frac * rms
+    if extra is not None:
+        bound = bound + extra
+    bound = np.maximum(bound, 1e-30)
+    ratio = np.abs(y_gpu - y_ref) / bound
+    worst = float(ratio.max()) if ratio.size else 0.0
+    if worst > 1.0:
+        i = np.unravel_index(np.argmax(ratio), ratio.shape)
+        raise AssertionError(f"parity fails at {i}: gpu={y_gpu[i]!r} ref={y_ref[i]!r} "
+                             f"ratio={worst:.3g}; {int((ratio > 1).sum())} of {ratio.size} fail")
+    return worst
+
+
+def sample_rows(M, count=48, seed=0):
+    """Rows spanning every 128-row tile edge, every 32-lane quadrant, plus random rows."""
+    rng = np.random.default_rng(seed)
+    fixed = {0, 31, 32, 63, 64, 95, 96, 127, M - 1, M - 128 if M > 128 else 0}
+    rows = set(r for r in fixed if 0 <= r < M)
+    while len(rows) < min(count, M):
+        rows.add(int(rng.integers(0, M)))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def oracle_y(inp, M, N, K, R, rows=None):
+    return oracle.forward(inp, M, N, K, R, rows=rows)

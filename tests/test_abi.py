@@ -1,0 +1,178 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol that
+include/svdq.h declares, validates arguments on the host, and plans
+launches (pipeline-depth solver, tensor-memory budget, persistent grid)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from nvfp4_w4a4_quantized_gb300 import binding, build
+from nvfp4_w4a4_quantized_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "svdq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(svdq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (svdq_\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for code in range(0, -9, -1):
+        s = binding.status_string(code)
+        assert s.startswith("SVDQ_")
+    assert binding.status_string(-99) == "SVDQ_ERR_UNKNOWN"
+    assert binding.svdq_version() >= 100
+
+
+# ---------------------------------------------------------------- validation
+A = 1 << 20  # fake, 16-byte aligned addresses: validation never dereferences
+
+
+def call(lib, M=256, N=256, K=256, R=32, ptrs=None, opts=None):
+    p = dict(act=A, wgt=A, ascales=A, wscales=A, la=A, lu=A, wc=A, bias=A, out=A)
+    p.update(ptrs or {})
+    args = [p["act"], p["wgt"], p["ascales"], p["wscales"], p["la"], p["lu"], p["wc"], p["bias"],
+            p["out"], M, N, K, R]
+    if opts is None:
+        return lib.svdq_w4a4_gemm(*args, None)
+    o = binding.SvdqOptions(**opts)
+    return lib.svdq_w4a4_gemm_ex(*args, ctypes.byref(o), None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(ptrs=dict(act=None)), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(ptrs=dict(out=None)), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(ptrs=dict(la=None)), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(ptrs=dict(lu=None)), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(M=-16), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(K=0), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(R=-1), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(M=24), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (dict(N=40), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (dict(K=96), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (dict(R=129), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (dict(K=(1 << 20) + 64), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (dict(M=(1 << 24) + 16), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (dict(ptrs=dict(act=A + 8)), binding.SVDQ_ERR_MISALIGNED),
+    (dict(ptrs=dict(wscales=A + 1)), binding.SVDQ_ERR_MISALIGNED),
+    (dict(ptrs=dict(out=A + 2)), binding.SVDQ_ERR_MISALIGNED),
+    (dict(ptrs=dict(bias=A + 2)), binding.SVDQ_ERR_MISALIGNED),
+    (dict(opts=dict(tile_n=64)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(stages=1)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(stages=9)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(debug_fault=2)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(reserved=(ctypes.c_int32 * 2)(0, 1))), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(cta_group=3)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(cta_group=2, tile_n=128)), binding.SVDQ_ERR_BAD_OPTION),
+])
+def test_host_validation(lib, kw, expect):
+    assert call(lib, **kw) == expect
+
+
+def test_rank_zero_needs_no_lora_pointers(lib):
+    # R == 0 with NULL LoRA pointers passes validation; the empty M makes it a no-op
+    assert call(lib, M=0, R=0, ptrs=dict(la=None, lu=None)) == binding.SVDQ_OK
+
+
+def test_empty_product_is_a_no_op(lib):
+    assert call(lib, M=0) == binding.SVDQ_OK
+    assert call(lib, N=0) == binding.SVDQ_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_no_device_is_reported(lib):
+    assert call(lib) == binding.SVDQ_ERR_UNSUPPORTED_DEVICE
+
+
+# ---------------------------------------------------------------- planner
+SMS = 152
+
+
+@pytest.mark.parametrize("w", [synth.TINY, synth.ATTN_PROJ, synth.MLP_UP, synth.MLP_DOWN]
+                         + synth.sweep_workloads(), ids=lambda w: w.name)
+def test_plan_budgets(lib, w):
+    plan = binding.svdq_query_plan(w.M, w.N, w.K, w.R, sm_count=SMS)
+    assert plan["tmem_cols_used"] <= plan["tmem_cols"] == 512
+    assert plan["smem_bytes"] <= 232448
+    assert plan["num_acc_stage"] == (1 if plan["tile_n"] == 256 else 2)
+    cg = plan["cta_group"]
+    assert plan["tile_m"] == 128 * cg
+    # a LoRA ring item (LA', LU', raw LA, wcscale, both operands split across
+    # a pair) fits inside one stage, so LoRA never costs pipeline depth
+    assert plan["lora_block_bytes"] <= plan["stage_bytes"]
+    assert plan["lora_blocks"] == -(-w.R // 32)
+    assert plan["k_blocks"] == -(-w.K // 256)
+    # pipeline depth: never silently clamped below 4 K-blocks in flight
+    assert plan["num_ab_stage"] >= 4
+    tiles = -(-w.M // plan["tile_m"]) * -(-w.N // plan["tile_n"])
+    assert plan["num_tiles"] == tiles
+    assert plan["grid"] == cg * min(tiles, SMS // cg)
+
+
+@pytest.mark.parametrize("cg,tn", [(1, 128), (1, 256), (2, 256)])
+def test_plan_each_tile_config(lib, cg, tn):
+    p = binding.svdq_query_plan(4096, 3072, 3072, 32, options=dict(cta_group=cg, tile_n=tn),
+                                sm_count=SMS)
+    assert (p["cta_group"], p["tile_n"], p["tile_m"]) == (cg, tn, 128 * cg)
+    # per-CTA stage: A rows 128 x 128 B, B rows (tile_n / cg) x 128 B, raw scale boxes
+    assert p["stage_bytes"] == 128 * 128 + (tn // cg) * 128 + 16 * 128 + 16 * tn
+    assert p["num_ab_stage"] >= 3
+    assert p["smem_bytes"] + p["stage_bytes"] > 232448 or p["num_ab_stage"] == 8 or \
+        p["tmem_cols_used"] + (16 + 16 * (tn // 128)) > 512   # the solver took all it could
+
+
+def test_plan_depth_independent_of_rank(lib):
+    depths = {binding.svdq_query_plan(4096, 3072, 12288, R, sm_count=SMS)["num_ab_stage"]
+              for R in (0, 16, 32, 64, 128)}
+    assert len(depths) == 1
+
+
+def test_plan_options(lib):
+    p = binding.svdq_query_plan(4096, 3072, 3072, 32, options=dict(tile_n=128, stages=3,
+                                                                  max_ctas=7), sm_count=SMS)
+    assert (p["tile_n"], p["cta_group"], p["num_ab_stage"], p["grid"]) == (128, 1, 3, 7)
+    p = binding.svdq_query_plan(4096, 3072, 3072, 32, options=dict(cta_group=2, max_ctas=7),
+                                sm_count=SMS)
+    assert p["grid"] == 6          # whole CTA pairs only
+    with pytest.raises(binding.SvdqError):
+        binding.svdq_query_plan(4096, 3072, 3072, 32, options=dict(tile_n=256, stages=8),
+                                sm_count=SMS)
+    # small problems fall back to single-CTA tiles
+    assert binding.svdq_query_plan(128, 3072, 3072, 32, sm_count=SMS)["cta_group"] == 1
+
+
+def test_lora_stage_bytes_match_the_pages_probe(lib):
+    # "SVDQuant W4A4 on Blackwell" §7.4: 2-CTA, R=128, 16-bit LoRA operands,
+    # mma tile (256, 128): per-CTA la_one = 32768 B and lu_one = 16384 B.
+    tot, la, lu = binding.svdq_lora_stage_bytes(256, 128, 128, 2, 2)
+    assert (la, lu, tot) == (32768, 16384, 49152)
+    # single CTA: nothing is split
+    assert binding.svdq_lora_stage_bytes(128, 256, 32, 2, 1)[1:] == (8192, 16384)
+    with pytest.raises(binding.SvdqError):
+        binding.svdq_lora_stage_bytes(255, 128, 128, 2, 2)
