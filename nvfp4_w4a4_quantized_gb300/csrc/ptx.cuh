@@ -229,7 +229,18 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Arrive on an mbarrier given by a shared::cluster address (possibly another CTA's).
+// Arrive on an mbarrier given by a shared::cluster address (this CTA's or the
+// pair peer's) with CTA-scope release.  Used where the arrival publishes
+// tensor-memory work (completed by tcgen05.wait::st / wait::ld and ordered by
+// tcgen05.fence::before_thread_sync) or nothing at all; it costs no more than a
+// local arrive.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+// Arrive with cluster-scope release: publishes this thread's generic
+// shared-memory writes to the other CTA of the pair.  Markedly slower (the
+// release stalls the issuing warp), so used only where that is needed.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");

@@ -13,11 +13,13 @@
 // 128 output rows; in a pair the leader (cluster rank 0) issues every MMA,
 // A is split along M and B along N between the two CTAs' shared memory.
 //
-// 12 warps per CTA:
-//   warp 0       TMA producer.  Main ring item (one 256-wide K block): packed
-//                act/wgt tiles (128-byte swizzle) and the raw [16 groups x rows]
-//                scale boxes.  LoRA ring item (32 ranks): raw fp32 LA rows,
-//                bf16 LU rows (64-byte swizzle) and wcscale.
+// 13 warps per CTA:
+//   warps 0, 12  TMA producers, taking alternate ring items (one issuing
+//                thread streams far fewer bytes per second than two).  Main
+//                ring item (one 256-wide K block): packed act/wgt tiles
+//                (128-byte swizzle) and the raw [16 groups x rows] scale boxes.
+//                LoRA ring item (32 ranks): raw fp32 LA rows, bf16 LU rows
+//                (64-byte swizzle) and wcscale.
 //   warp 1       MMA issuer (one thread, leader CTA): tcgen05.mma kind::mxf4nvf4
 //                block_scale.scale_vec::4X for main items, kind::f16 (bf16) for
 //                LoRA items, commits that free ring stages / publish accumulators.
@@ -39,8 +41,8 @@
 //
 // Every mbarrier wait is bounded by %globaltimer; on expiry the kernel records
 // SVDQ_ERR_TIMEOUT and the wait site, every role leaves its loop, in-flight
-// TMA and tcgen05 work is drained with a second bounded wait, tensor memory is
-// freed and the CTA exits.
+// tcgen05 work is drained with a second bounded wait, in-flight TMA loads get
+// a fixed grace period, tensor memory is freed and the CTA exits.
 #pragma once
 
 #include <cuda.h>
@@ -51,7 +53,7 @@
 
 namespace svdq {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 416;
 constexpr int kBM = 128;     // output rows per CTA (per-CTA MMA M)
 constexpr int kBK = 256;     // K elements per main ring item (128 packed bytes per row)
 constexpr int kLoraRanks = 32;  // ranks per LoRA ring item
@@ -146,6 +148,18 @@ __device__ __forceinline__ void tile_coords(const KParams& p, int t, int& mb, in
   nb = local / gsz;
 }
 
+// K-block visiting order of a tile: tiles that share an A or a B block start
+// their K sweep at different blocks, so the clusters reading one operand block
+// at the same time do not all wait on the same first-touch DRAM fetch.  Only
+// the fp32 accumulation order changes.
+__device__ __forceinline__ int k_rotation(const KParams& p, int mb, int nb) {
+  return (7 * mb + 5 * nb) % p.k_blocks;
+}
+__device__ __forceinline__ int k_block(const KParams& p, int main_item, int rot) {
+  const int kb = main_item + rot;
+  return kb >= p.k_blocks ? kb - p.k_blocks : kb;
+}
+
 struct Ctl {
   volatile int* abort_flag;
   int* status;
@@ -161,11 +175,12 @@ __device__ __noinline__ void report_timeout(int* status, int site) {
 
 // Bounded wait for the phase with parity `parity` of a local mbarrier.
 // Returns false (and makes every other role of this CTA give up) on expiry or
-// if another role already gave up.
-template <int CG>
+// if another role already gave up.  CLUSTER selects a cluster-scope acquire,
+// needed on the pair leader's barriers that receive the peer's arrivals.
+template <bool CLUSTER>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int site, const Ctl& c) {
   auto probe = [&]() {
-    return CG == 2 ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    return CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
   };
   if (probe()) return true;
   const uint64_t t0 = ptx::globaltimer();
@@ -180,10 +195,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int site
   }
 }
 
-template <int CG>
+template <bool CLUSTER>
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, int site,
                                               const Ctl& c) {
-  const bool ok = wait_bar<CG>(bar, parity, site, c);
+  const bool ok = wait_bar<CLUSTER>(bar, parity, site, c);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -408,12 +423,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 12) {
+    // ------------------------------------------------------------ producers
     if (lane == 0) {
+      const int who = warp == 0 ? 0 : 1;  // this thread issues ring items j with j % 2 == who
       int stage = 0;
       uint32_t phase = 0;
-      long long issued = 0;
+      long long j = 0;
       bool ok = true;
       const uint32_t main_aux_bytes = 16 * kBM + 16 * BN;
       const uint32_t lora_aux_bytes =
@@ -424,57 +440,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = mb * kBM * CG, n0 = nb * BN;
         const int m_cta = m0 + kBM * static_cast<int>(rank);
         const int n_cta = n0 + L::kBNc * static_cast<int>(rank);
-        for (int i = 0; i < n_items; ++i) {
-          if (!wait_bar<CG>(empty(stage), phase ^ 1u, kSiteProducerEmpty, ctl)) {
-            ok = false;
-            break;
-          }
-          const uint32_t st = sbase + stage * L::kStageBytes;
-          if (i < p.lora_blocks) {
-            if (p.lora_tma) {
-              ptx::mbar_arrive_expect_tx(auxfull(stage), lora_aux_bytes);
-              ptx::tma_load_2d(st + L::kLoraRawLA, &tm_la, auxfull(stage), kLoraRanks * i, m_cta);
-              ptx::tma_load_2d(st + L::kLoraLU, &tm_lu, auxfull(stage), kLoraRanks * i, n_cta);
-              if (p.wcscale != nullptr)
-                ptx::tma_load_1d(st + L::kLoraWC, &tm_wc, auxfull(stage), n_cta);
-            } else {
-              ptx::mbar_arrive(auxfull(stage));
+        const int rot = k_rotation(p, mb, nb);
+        for (int i = 0; i < n_items; ++i, ++j) {
+          if ((j & 1) == who) {
+            if (!wait_bar<false>(empty(stage), phase ^ 1u, kSiteProducerEmpty, ctl)) {
+              ok = false;
+              break;
             }
-            if (leader) ptx::mbar_arrive(full(stage));
-          } else {
-            const int kb = i - p.lora_blocks;
-            ptx::mbar_arrive_expect_tx(auxfull(stage), main_aux_bytes);
-            ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, auxfull(stage), m_cta, kb * 16);
-            ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, auxfull(stage), n0, kb * 16);
-            if (leader) ptx::mbar_arrive_expect_tx(full(stage), CG * (L::kOffSFA - L::kOffA));
-            if (CG == 2) {
-              const uint32_t fb = to_leader(full(stage));
-              ptx::tma_load_2d_pair(st + L::kOffA, &tm_act, fb, kb * 128, m_cta);
-              ptx::tma_load_2d_pair(st + L::kOffB, &tm_wgt, fb, kb * 128, n_cta);
+            const uint32_t st = sbase + stage * L::kStageBytes;
+            if (i < p.lora_blocks) {
+              if (p.lora_tma) {
+                ptx::mbar_arrive_expect_tx(auxfull(stage), lora_aux_bytes);
+                ptx::tma_load_2d(st + L::kLoraRawLA, &tm_la, auxfull(stage), kLoraRanks * i, m_cta);
+                ptx::tma_load_2d(st + L::kLoraLU, &tm_lu, auxfull(stage), kLoraRanks * i, n_cta);
+                if (p.wcscale != nullptr)
+                  ptx::tma_load_1d(st + L::kLoraWC, &tm_wc, auxfull(stage), n_cta);
+              } else {
+                ptx::mbar_arrive(auxfull(stage));
+              }
+              if (leader) ptx::mbar_arrive(full(stage));
             } else {
-              ptx::tma_load_2d(st + L::kOffA, &tm_act, full(stage), kb * 128, m_cta);
-              ptx::tma_load_2d(st + L::kOffB, &tm_wgt, full(stage), kb * 128, n_cta);
+              const int kb = k_block(p, i - p.lora_blocks, rot);
+              ptx::mbar_arrive_expect_tx(auxfull(stage), main_aux_bytes);
+              ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, auxfull(stage), m_cta, kb * 16);
+              ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, auxfull(stage), n0, kb * 16);
+              if (leader) ptx::mbar_arrive_expect_tx(full(stage), CG * (L::kOffSFA - L::kOffA));
+              if (CG == 2) {
+                const uint32_t fb = to_leader(full(stage));
+                ptx::tma_load_2d_pair(st + L::kOffA, &tm_act, fb, kb * 128, m_cta);
+                ptx::tma_load_2d_pair(st + L::kOffB, &tm_wgt, fb, kb * 128, n_cta);
+              } else {
+                ptx::tma_load_2d(st + L::kOffA, &tm_act, full(stage), kb * 128, m_cta);
+                ptx::tma_load_2d(st + L::kOffB, &tm_wgt, full(stage), kb * 128, n_cta);
+              }
             }
           }
-          ++issued;
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // No TMA write may still be landing in this CTA's shared memory at exit.
-      for (long long j = (issued > S ? issued - S : 0); j < issued; ++j) {
-        const int s = static_cast<int>(j % S);
-        const uint32_t par = static_cast<uint32_t>((j / S) & 1);
-        drain_wait(auxfull(s), par);
-        if (leader) drain_wait(full(s), par);
-      }
-      if (CG == 2 && !leader && !ok) {
-        // The pair's operand loads signal the leader's barriers; after an abort
-        // give any still-landing load a fixed grace period.
+      // On the normal path every load has been consumed before the teardown
+      // barrier.  After an abort a load may still be landing in this CTA's
+      // shared memory (or signalling the pair leader): give it a fixed grace
+      // period before the CTA can exit.
+      if (!ok) {
         const uint64_t t0 = ptx::globaltimer();
-        while (ptx::globaltimer() - t0 < 100000ull) {
+        while (ptx::globaltimer() - t0 < 200000ull) {
         }
       }
     }
@@ -489,12 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescMain = ptx::idesc_mxf4nvf4(kBM * CG, BN);
       constexpr uint32_t kIdescLora = ptx::idesc_bf16_f32(kBM * CG, BN);
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++tile_iter) {
+        int mb, nb;
+        tile_coords(p, t, mb, nb);
+        const int rot = k_rotation(p, mb, nb);
         const int acc_stage = tile_iter % L::kAccStages;
         const uint32_t acc_phase = static_cast<uint32_t>(tile_iter / L::kAccStages) & 1u;
         // A free accumulator: the epilogue released this buffer's previous tile.
         // (debug_fault inverts the expected phase -- the single-stage
         // "producer must start at phase 1" mistake -- so the wait expires.)
-        if (!wait_bar<CG>(acc_empty(acc_stage), acc_phase ^ 1u ^ (p.debug_fault ? 1u : 0u),
+        if (!wait_bar<CG == 2>(acc_empty(acc_stage), acc_phase ^ 1u ^ (p.debug_fault ? 1u : 0u),
                           kSiteMmaAccEmpty, ctl)) {
           ok = false;
           break;
@@ -503,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc_stage * BN);
         uint32_t accumulate = 0;
         for (int i = 0; i < n_items; ++i) {
-          if (!wait_bar<CG>(full(stage), phase, kSiteMmaFull, ctl) ||
-              !wait_bar<CG>(ready(stage), phase, kSiteMmaReady, ctl)) {
+          if (!wait_bar<CG == 2>(full(stage), phase, kSiteMmaFull, ctl) ||
+              !wait_bar<CG == 2>(ready(stage), phase, kSiteMmaReady, ctl)) {
             ok = false;
             break;
           }
@@ -532,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mma_commit_pair(lora_done);
               else
                 ptx::mma_commit(lora_done);
-              if (!wait_bar<CG>(lora_done, lora_phase, kSiteMmaLoraDone, ctl)) {
+              if (!wait_bar<false>(lora_done, lora_phase, kSiteMmaLoraDone, ctl)) {
                 ok = false;
                 break;
               }
@@ -540,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tc_fence_after();
             }
           } else {
-            const int kb = i - p.lora_blocks;
+            const int kb = k_block(p, i - p.lora_blocks, rot);
             const uint32_t sf =
                 tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
             const int nsteps = min(4, (p.K - kb * kBK) / 64);
@@ -590,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_cta = nb * BN + L::kBNc * static_cast<int>(rank);
       bool ok = true;
       for (int i = 0; i < n_items; ++i) {
-        if (!warp_wait_bar<CG>(auxfull(stage), phase, kSiteLoraAuxFull, ctl)) {
+        if (!warp_wait_bar<false>(auxfull(stage), phase, kSiteLoraAuxFull, ctl)) {
           ok = false;
           break;
         }
@@ -610,7 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_cluster(ready_bar0 + 8u * stage);
+        if (lane == 0) {
+          // The pair peer's LoRA operands are generic shared-memory writes the
+          // leader's MMA reads: publish them with a cluster-scope release.
+          if (CG == 2 && !leader && i < p.lora_blocks)
+            ptx::mbar_arrive_cluster(ready_bar0 + 8u * stage);
+          else
+            ptx::mbar_arrive_remote(ready_bar0 + 8u * stage);
+        }
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
@@ -641,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int acc_stage = tile_iter % L::kAccStages;
       const uint32_t acc_phase = static_cast<uint32_t>(tile_iter / L::kAccStages) & 1u;
-      if (!warp_wait_bar<CG>(acc_full(acc_stage), acc_phase, kSiteEpiAccFull, ctl)) break;
+      if (!warp_wait_bar<false>(acc_full(acc_stage), acc_phase, kSiteEpiAccFull, ctl)) break;
       ptx::tc_fence_after();
       if (lane < BN / 8) {
         *reinterpret_cast<uint4*>(wcb + 16 * lane) = wv;
@@ -688,11 +711,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(acc_empty0 + 8u * acc_stage);
+      if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
     }
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();
-  } else {
+  } else if (warp < 12) {
     // ------------------------------------------------------------ scale feeders
     const int q = warp & 3;
     int stage = 0;
@@ -702,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
       bool ok = true;
       for (int i = 0; i < n_items; ++i) {
-        if (!warp_wait_bar<CG>(auxfull(stage), phase, kSiteSfAuxFull, ctl)) {
+        if (!warp_wait_bar<false>(auxfull(stage), phase, kSiteSfAuxFull, ctl)) {
           ok = false;
           break;
         }
@@ -713,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           sf_relayout<L::kSfbHalves>(st + L::kOffSFB + 4 * BN * q, lane);
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(sft);
-          if (!warp_wait_bar<CG>(sft, sft_phase, kSiteSfTranspose, ctl)) {
+          if (!warp_wait_bar<false>(sft, sft_phase, kSiteSfTranspose, ctl)) {
             ok = false;
             break;
           }
@@ -741,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_before();
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_cluster(ready_bar0 + 8u * stage);
+        if (lane == 0) ptx::mbar_arrive_remote(ready_bar0 + 8u * stage);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
