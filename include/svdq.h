@@ -111,12 +111,12 @@ int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* ascales, con
 typedef struct svdq_plan {
     int32_t tile_m, tile_n, tile_k;  /* output tile per cluster and K per ring item  */
     int32_t cta_group;               /* CTAs sharing one MMA (1 or 2)                */
-    int32_t num_ab_stage;            /* ring depth (K-blocks in flight)              */
+    int32_t num_ab_stage;            /* ring depth (stages in flight)                */
     int32_t num_acc_stage;           /* accumulator buffers in tensor memory         */
     int32_t stage_bytes;             /* shared-memory bytes per ring stage, per CTA  */
     int32_t lora_block_bytes;        /* LoRA operand bytes per ring item, per CTA    */
-    int32_t lora_blocks;             /* LoRA ring items per tile (R padded to 64)    */
-    int32_t k_blocks;                /* main ring items per tile                     */
+    int32_t lora_blocks;             /* LoRA ring items per tile (32 ranks each)     */
+    int32_t k_blocks;                /* 256-wide K blocks per tile                   */
     int32_t smem_bytes;              /* dynamic shared memory per CTA                */
     int32_t tmem_cols;               /* tensor-memory columns allocated per CTA      */
     int32_t tmem_cols_used;          /* of which used                                */
@@ -124,6 +124,7 @@ typedef struct svdq_plan {
     int64_t num_tiles;               /* output tiles                                 */
     int32_t grid;                    /* persistent CTAs launched                     */
     int32_t sm_count;                /* SMs the grid was sized for                   */
+    int32_t kblocks_per_stage;       /* 256-wide K blocks carried by one ring stage  */
 } svdq_plan_t;
 
 /* Fill *plan for the given shape.  sm_count <= 0 queries the current device

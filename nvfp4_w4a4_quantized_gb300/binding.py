@@ -45,7 +45,8 @@ class SvdqPlan(ctypes.Structure):
                 ("k_blocks", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("tmem_cols", ctypes.c_int32), ("tmem_cols_used", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("num_tiles", ctypes.c_int64),
-                ("grid", ctypes.c_int32), ("sm_count", ctypes.c_int32)]
+                ("grid", ctypes.c_int32), ("sm_count", ctypes.c_int32),
+                ("kblocks_per_stage", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

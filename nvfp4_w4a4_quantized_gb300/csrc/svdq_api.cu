@@ -48,6 +48,8 @@ struct Plan {
   int lora_block_bytes = 0;
   int lora_blocks = 0;
   int k_blocks = 0;
+  int main_items = 0;
+  int kbi = 1;
   int r16 = 0;
   int smem_bytes = 0;
   int tmem_cols_used = 0;
@@ -81,17 +83,25 @@ int validate_shape(int64_t M, int64_t N, int64_t K, int64_t R) {
 
 // Per-(CTA group, tile) constants the solver needs.
 struct TileInfo {
-  int stage_bytes, acc_cols, sf_cols, acc_stages, fixed_smem, lora_block_bytes;
+  int stage_bytes, acc_cols, sf_cols, acc_stages, fixed_smem, lora_block_bytes, kbi;
 };
+
+// K blocks per main ring item: the CTA pair's stages are small enough to
+// carry two K blocks each (two stages fit); single-CTA tiles keep one.
+template <int CG>
+constexpr int kbi_for() {
+  return CG == 2 ? 2 : 1;
+}
 
 template <int CG, int BN>
 TileInfo tile_info() {
-  using L = Layout<CG, BN>;
+  using L = Layout<CG, BN, kbi_for<CG>()>;
   // LoRA ring item: LA' [128][32] bf16 + LU' [BN/CG][32] bf16 + raw LA [128][32] fp32
   // + wcscale; all inside one stage (both operands divided across a pair).
   return TileInfo{L::kStageBytes, L::kAccCols, L::kSfCols, L::kAccStages, L::smem_bytes(0),
                   kBM * kLoraRanks * 2 + L::kBNc * kLoraRanks * 2 + kBM * kLoraRanks * 4 +
-                      2 * L::kBNc};
+                      2 * L::kBNc,
+                  L::kKbi};
 }
 
 TileInfo tile_info_for(int cg, int bn) {
@@ -137,6 +147,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* 
   pl.tmem_cols_used = ti.acc_cols + pl.stages * ti.sf_cols;
   pl.lora_block_bytes = ti.lora_block_bytes;
   pl.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
+  pl.kbi = ti.kbi;
+  pl.main_items = (pl.k_blocks + pl.kbi - 1) / pl.kbi;
   pl.lora_blocks = static_cast<int>((R + kLoraRanks - 1) / kLoraRanks);
   pl.r16 = static_cast<int>((R + 15) / 16 * 16);
   const int tm = kBM * pl.cta_group;
@@ -215,7 +227,7 @@ int ensure_kernel(DeviceInfo* d, int smem_bytes) {
   std::lock_guard<std::mutex> lock(g_mutex);
   const int idx = kernel_index<CG, BN>();
   if (!d->attr_set[idx]) {
-    auto k = svdq_w4a4_kernel<CG, BN>;
+    auto k = svdq_w4a4_kernel<CG, BN, kbi_for<CG>()>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -266,7 +278,8 @@ struct Operands {
 template <int CG, int BN>
 int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams& kp, int64_t M,
            int64_t N, int64_t K, int64_t R, cudaStream_t stream) {
-  using L = Layout<CG, BN>;
+  constexpr int KBI = kbi_for<CG>();
+  using L = Layout<CG, BN, KBI>;
   (void)dinfo;
   int rc = SVDQ_OK;
   alignas(64) CUtensorMap tm[8];
@@ -284,13 +297,13 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
       return rc;
     const uint64_t d_sfa[2] = {static_cast<uint64_t>(M), static_cast<uint64_t>(K / 16)},
                    s_sfa[1] = {static_cast<uint64_t>(M)};
-    const uint32_t b_sfa[2] = {kBM, 16};
+    const uint32_t b_sfa[2] = {kBM, 16 * KBI};
     if ((rc = encode(&tm[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.ascales, d_sfa, s_sfa, b_sfa,
                      CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
       return rc;
     const uint64_t d_sfb[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K / 16)},
                    s_sfb[1] = {static_cast<uint64_t>(N)};
-    const uint32_t b_sfb[2] = {BN, 16};
+    const uint32_t b_sfb[2] = {BN, 16 * KBI};
     if ((rc = encode(&tm[3], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.wscales, d_sfb, s_sfb, b_sfb,
                      CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
       return rc;
@@ -339,7 +352,7 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CG == 2 ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, svdq_w4a4_kernel<CG, BN>, tm[0], tm[1], tm[2],
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, svdq_w4a4_kernel<CG, BN, KBI>, tm[0], tm[1], tm[2],
                                            tm[3], tm[4], tm[5], tm[6], tm[7], kp);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -401,6 +414,7 @@ extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* a
   kp.num_tiles = static_cast<int>(pl.num_tiles);
   kp.group_m = pl.group_m;
   kp.k_blocks = pl.k_blocks;
+  kp.main_items = pl.main_items;
   kp.lora_blocks = pl.lora_blocks;
   kp.r16 = pl.r16;
   kp.num_stages = pl.stages;
@@ -464,6 +478,7 @@ extern "C" int svdq_query_plan(int64_t M, int64_t N, int64_t K, int64_t R,
   plan->num_tiles = pl.num_tiles;
   plan->grid = pl.grid;
   plan->sm_count = sm_count;
+  plan->kblocks_per_stage = pl.kbi;
   return SVDQ_OK;
 }
 

@@ -55,7 +55,7 @@ namespace svdq {
 
 constexpr int kThreads = 416;
 constexpr int kBM = 128;     // output rows per CTA (per-CTA MMA M)
-constexpr int kBK = 256;     // K elements per main ring item (128 packed bytes per row)
+constexpr int kBK = 256;     // K elements per K block (128 packed bytes per row)
 constexpr int kLoraRanks = 32;  // ranks per LoRA ring item
 constexpr int kMaxStages = 8;
 constexpr int kTmemCols = 512;
@@ -75,17 +75,26 @@ enum WaitSite : int {
 
 constexpr int kStatusTimeout = -7;  // == SVDQ_ERR_TIMEOUT
 
-template <int CG, int BN>
+// CG: CTAs per MMA; BN: tile columns; KBI: K blocks (of 256) per main ring
+// item.  Larger items halve the fixed per-item costs (one TMA batch, one
+// barrier round trip, one scale hand-off per item) at the price of fewer,
+// larger ring stages.
+template <int CG, int BN, int KBI>
 struct Layout {
   static_assert(CG == 1 || CG == 2, "CTA group is 1 or 2");
   static_assert(BN == 128 || BN == 256, "tile_n is 128 or 256");
   static_assert(!(CG == 2 && BN == 128), "a CTA pair uses 256-wide tiles");
-  static constexpr int kBNc = BN / CG;                // B rows held by this CTA
-  static constexpr int kOffA = 0;                     // 128 rows x 128 B
-  static constexpr int kOffB = kBM * 128;             // kBNc rows x 128 B
-  static constexpr int kOffSFA = kOffB + kBNc * 128;  // raw [16 groups][128 rows]
-  static constexpr int kOffSFB = kOffSFA + 16 * kBM;  // raw [16 groups][BN cols] (whole N tile)
-  static constexpr int kStageBytes = kOffSFB + 16 * BN;
+  static_assert(KBI == 1 || KBI == 2, "one or two K blocks per ring item");
+  static constexpr int kKbi = KBI;
+  static constexpr int kSteps = 4 * KBI;                    // K=64 MMA steps per item
+  static constexpr int kBNc = BN / CG;                      // B rows held by this CTA
+  static constexpr int kATile = kBM * 128;                  // one K block of A: 128 rows x 128 B
+  static constexpr int kBTile = kBNc * 128;                 // one K block of B
+  static constexpr int kOffA = 0;                           // KBI A tiles
+  static constexpr int kOffB = KBI * kATile;                // KBI B tiles
+  static constexpr int kOffSFA = kOffB + KBI * kBTile;      // raw [16*KBI groups][128 rows]
+  static constexpr int kOffSFB = kOffSFA + 16 * KBI * kBM;  // raw [16*KBI groups][BN] (whole N tile)
+  static constexpr int kStageBytes = kOffSFB + 16 * KBI * BN;
   static constexpr int kSfbHalves = BN / 128;
   // LoRA item: LA' [128][32] bf16 and LU' [kBNc][32] bf16 (64-byte rows,
   // 64-byte swizzle), raw LA [128][32] fp32, wcscale [kBNc] bf16.
@@ -98,7 +107,8 @@ struct Layout {
   static_assert(2 * kBNc <= 16 * kBM, "wcscale fits the scale area");
   static constexpr int kAccStages = (BN == 256) ? 1 : 2;
   static constexpr int kAccCols = kAccStages * BN;
-  static constexpr int kSfCols = 16 + 16 * kSfbHalves;  // tensor-memory scale columns per stage
+  // tensor-memory scale columns per stage: SFA 4 per K step, then SFB 4*halves per K step
+  static constexpr int kSfCols = kSteps * (4 + 4 * kSfbHalves);
   static constexpr int kEpiStageBytes = 32 * 64;        // one 32 x 32 bf16 output tile
   static constexpr int kEpiBytes = 4 * 2 * kEpiStageBytes;
   static constexpr int kWcbBytes = 4 * 2 * BN * 2;      // per epilogue warp: wc[BN], bias[BN]
@@ -124,6 +134,7 @@ struct KParams {
   int M, N, K, R;
   int tiles_m, tiles_n, num_tiles, group_m;
   int k_blocks;     // ceil(K / 256)
+  int main_items;   // ceil(k_blocks / K blocks per item)
   int lora_blocks;  // ceil(R / 32)
   int r16;          // R rounded up to 16
   int num_stages;
@@ -148,16 +159,16 @@ __device__ __forceinline__ void tile_coords(const KParams& p, int t, int& mb, in
   nb = local / gsz;
 }
 
-// K-block visiting order of a tile: tiles that share an A or a B block start
-// their K sweep at different blocks, so the clusters reading one operand block
+// Main-item visiting order of a tile: tiles that share an A or a B block start
+// their K sweep at different items, so the clusters reading one operand block
 // at the same time do not all wait on the same first-touch DRAM fetch.  Only
 // the fp32 accumulation order changes.
 __device__ __forceinline__ int k_rotation(const KParams& p, int mb, int nb) {
-  return (7 * mb + 5 * nb) % p.k_blocks;
+  return (7 * mb + 5 * nb) % p.main_items;
 }
-__device__ __forceinline__ int k_block(const KParams& p, int main_item, int rot) {
-  const int kb = main_item + rot;
-  return kb >= p.k_blocks ? kb - p.k_blocks : kb;
+__device__ __forceinline__ int k_item(const KParams& p, int main_item, int rot) {
+  const int it = main_item + rot;
+  return it >= p.main_items ? it - p.main_items : it;
 }
 
 struct Ctl {
@@ -342,7 +353,7 @@ __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p, i
   }
 }
 
-template <int CG, int BN>
+template <int CG, int BN, int KBI>
 __global__ void __launch_bounds__(kThreads, 1)
     svdq_w4a4_kernel(const __grid_constant__ CUtensorMap tm_act,
                      const __grid_constant__ CUtensorMap tm_wgt,
@@ -352,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_lu,
                      const __grid_constant__ CUtensorMap tm_wc,
                      const __grid_constant__ CUtensorMap tm_out, const KParams p) {
-  using L = Layout<CG, BN>;
+  using L = Layout<CG, BN, KBI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -360,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = static_cast<int>(threadIdx.x) / 32;
   const int lane = static_cast<int>(threadIdx.x) % 32;
   const int S = p.num_stages;
-  const int n_items = p.lora_blocks + p.k_blocks;
+  const int n_items = p.lora_blocks + p.main_items;
   const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
   const bool leader = (rank == 0);
   const int cluster_id = static_cast<int>(blockIdx.x) / CG;
@@ -431,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       long long j = 0;
       bool ok = true;
-      const uint32_t main_aux_bytes = 16 * kBM + 16 * BN;
+      const uint32_t main_aux_bytes = 16 * KBI * (kBM + BN);
       const uint32_t lora_aux_bytes =
           kBM * kLoraRanks * 4 + L::kBNc * 64 + (p.wcscale != nullptr ? 2 * L::kBNc : 0);
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
@@ -460,18 +471,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               if (leader) ptx::mbar_arrive(full(stage));
             } else {
-              const int kb = k_block(p, i - p.lora_blocks, rot);
+              const int kb0 = KBI * k_item(p, i - p.lora_blocks, rot);
+              const int nkb = min(KBI, p.k_blocks - kb0);
               ptx::mbar_arrive_expect_tx(auxfull(stage), main_aux_bytes);
-              ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, auxfull(stage), m_cta, kb * 16);
-              ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, auxfull(stage), n0, kb * 16);
-              if (leader) ptx::mbar_arrive_expect_tx(full(stage), CG * (L::kOffSFA - L::kOffA));
-              if (CG == 2) {
-                const uint32_t fb = to_leader(full(stage));
-                ptx::tma_load_2d_pair(st + L::kOffA, &tm_act, fb, kb * 128, m_cta);
-                ptx::tma_load_2d_pair(st + L::kOffB, &tm_wgt, fb, kb * 128, n_cta);
-              } else {
-                ptx::tma_load_2d(st + L::kOffA, &tm_act, full(stage), kb * 128, m_cta);
-                ptx::tma_load_2d(st + L::kOffB, &tm_wgt, full(stage), kb * 128, n_cta);
+              ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, auxfull(stage), m_cta, kb0 * 16);
+              ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, auxfull(stage), n0, kb0 * 16);
+              if (leader)
+                ptx::mbar_arrive_expect_tx(full(stage), CG * nkb * (L::kATile + L::kBTile));
+              for (int kk = 0; kk < nkb; ++kk) {
+                const int kx = (kb0 + kk) * 128;
+                const uint32_t da = st + L::kOffA + kk * L::kATile;
+                const uint32_t db = st + L::kOffB + kk * L::kBTile;
+                if (CG == 2) {
+                  const uint32_t fb = to_leader(full(stage));
+                  ptx::tma_load_2d_pair(da, &tm_act, fb, kx, m_cta);
+                  ptx::tma_load_2d_pair(db, &tm_wgt, fb, kx, n_cta);
+                } else {
+                  ptx::tma_load_2d(da, &tm_act, full(stage), kx, m_cta);
+                  ptx::tma_load_2d(db, &tm_wgt, full(stage), kx, n_cta);
+                }
               }
             }
           }
@@ -556,14 +574,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tc_fence_after();
             }
           } else {
-            const int kb = k_block(p, i - p.lora_blocks, rot);
+            const int kb0 = KBI * k_item(p, i - p.lora_blocks, rot);
             const uint32_t sf =
                 tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
-            const int nsteps = min(4, (p.K - kb * kBK) / 64);
-            for (int s = 0; s < nsteps; ++s) {
-              const uint64_t ad = ptx::desc_kmajor_sw128(st + L::kOffA + 32 * s);
-              const uint64_t bd = ptx::desc_kmajor_sw128(st + L::kOffB + 32 * s);
-              const uint32_t sfa = sf + 4 * s, sfb = sf + 16 + 4 * s * L::kSfbHalves;
+            // K=64 steps present in this item (the last K block may be partial)
+            const int nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
+            for (int ks = 0; ks < nsteps; ++ks) {
+              const int kk = ks >> 2, s = ks & 3;
+              const uint64_t ad = ptx::desc_kmajor_sw128(st + L::kOffA + kk * L::kATile + 32 * s);
+              const uint64_t bd = ptx::desc_kmajor_sw128(st + L::kOffB + kk * L::kBTile + 32 * s);
+              const uint32_t sfa = sf + 4 * ks;
+              const uint32_t sfb = sf + 4 * L::kSteps + 4 * ks * L::kSfbHalves;
               if (CG == 2)
                 ptx::mma_mxf4nvf4_pair(d_tmem, ad, bd, kIdescMain, sfa, sfb, accumulate);
               else
@@ -731,9 +752,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (i >= p.lora_blocks) {
           uint8_t* st = smem + stage * L::kStageBytes;
-          // this warp relayouts K-step q of the stage; the four warps then share
-          sf_relayout<1>(st + L::kOffSFA + 512 * q, lane);
-          sf_relayout<L::kSfbHalves>(st + L::kOffSFB + 4 * BN * q, lane);
+          // this warp relayouts K steps q, q+4, ... of the stage; the four warps
+          // then share the result
+#pragma unroll
+          for (int ks = q; ks < L::kSteps; ks += 4) {
+            sf_relayout<1>(st + L::kOffSFA + 512 * ks, lane);
+            sf_relayout<L::kSfbHalves>(st + L::kOffSFB + 4 * BN * ks, lane);
+          }
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(sft);
           if (!warp_wait_bar<false>(sft, sft_phase, kSiteSfTranspose, ctl)) {
@@ -742,24 +767,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           sft_phase ^= 1u;
           // row (32q + lane) of tensor memory: words j = rows lane + 32j of
-          // each 128-row block, for K-steps 0..3
-          uint32_t a[16], b[16 * L::kSfbHalves];
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint4 x = lds128(st + L::kOffSFA + 512 * s + 16 * lane);
-            a[4 * s] = x.x; a[4 * s + 1] = x.y; a[4 * s + 2] = x.z; a[4 * s + 3] = x.w;
-#pragma unroll
-            for (int h = 0; h < L::kSfbHalves; ++h) {
-              const uint4 y = lds128(st + L::kOffSFB + 4 * BN * s + 512 * h + 16 * lane);
-              const int o = 4 * (s * L::kSfbHalves + h);
-              b[o] = y.x; b[o + 1] = y.y; b[o + 2] = y.z; b[o + 3] = y.w;
-            }
-          }
+          // each 128-row block, four K steps (one K block) at a time
           const uint32_t col = tmem_base + lane_base +
                                static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
-          ptx::tmem_st_32x32b_x16(col, a);
 #pragma unroll
-          for (int h = 0; h < L::kSfbHalves; ++h) ptx::tmem_st_32x32b_x16(col + 16 + 16 * h, b + 16 * h);
+          for (int kk = 0; kk < KBI; ++kk) {
+            uint32_t a[16], b[16 * L::kSfbHalves];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const int ks = 4 * kk + s;
+              const uint4 x = lds128(st + L::kOffSFA + 512 * ks + 16 * lane);
+              a[4 * s] = x.x; a[4 * s + 1] = x.y; a[4 * s + 2] = x.z; a[4 * s + 3] = x.w;
+#pragma unroll
+              for (int h = 0; h < L::kSfbHalves; ++h) {
+                const uint4 y = lds128(st + L::kOffSFB + 4 * BN * ks + 512 * h + 16 * lane);
+                const int o = 4 * (s * L::kSfbHalves + h);
+                b[o] = y.x; b[o + 1] = y.y; b[o + 2] = y.z; b[o + 3] = y.w;
+              }
+            }
+            ptx::tmem_st_32x32b_x16(col + 16 * kk, a);
+#pragma unroll
+            for (int h = 0; h < L::kSfbHalves; ++h)
+              ptx::tmem_st_32x32b_x16(col + 4 * L::kSteps + 16 * L::kSfbHalves * kk + 16 * h,
+                                      b + 16 * h);
+          }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
         }
