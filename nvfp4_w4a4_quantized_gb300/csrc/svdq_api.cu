@@ -86,11 +86,12 @@ struct TileInfo {
   int stage_bytes, acc_cols, sf_cols, acc_stages, fixed_smem, lora_block_bytes, kbi;
 };
 
-// K blocks per main ring item: the CTA pair's stages are small enough to
-// carry two K blocks each (two stages fit); single-CTA tiles keep one.
+// K blocks per main ring item.  One: five single-block stages keep more
+// loads in flight than two double-block stages, and the MMA issuer's per-item
+// cost (one barrier wait, one commit) stays below four K=64 MMAs.
 template <int CG>
 constexpr int kbi_for() {
-  return CG == 2 ? 2 : 1;
+  return 1;
 }
 
 template <int CG, int BN>
@@ -256,13 +257,19 @@ int ensure_kernel(DeviceInfo* d, int smem_bytes) {
   return SVDQ_OK;
 }
 
+// rank 1..3; strides_bytes holds rank - 1 strides (dimensions 1..rank-1).
 int encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
            const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
            CUtensorMapSwizzle swz) {
-  cuuint64_t gd[2] = {dims[0], rank > 1 ? dims[1] : 1};
-  cuuint64_t gs[1] = {rank > 1 ? strides_bytes[0] : 0};
-  cuuint32_t bx[2] = {box[0], rank > 1 ? box[1] : 1};
-  const cuuint32_t es[2] = {1, 1};
+  cuuint64_t gd[3] = {1, 1, 1};
+  cuuint64_t gs[2] = {0, 0};
+  cuuint32_t bx[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    if (i > 0) gs[i - 1] = strides_bytes[i - 1];
+  }
+  const cuuint32_t es[3] = {1, 1, 1};
   const CUresult r =
       g_encode(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -284,15 +291,18 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
   int rc = SVDQ_OK;
   alignas(64) CUtensorMap tm[8];
   const uint64_t u = static_cast<uint64_t>(K / 2);
+  // Row-quad views of row-major [rows][width] operands: dims (width, rows / 4,
+  // 4) with strides (4 rows, 1 row).  A box (w, 32, 4) lands in shared memory
+  // as 128 rows in which row a + 32b is matrix row 4a + b of the block.
+  const uint64_t M4 = static_cast<uint64_t>(M / 4), N4 = static_cast<uint64_t>(N / 4);
   {
-    const uint64_t d_act[2] = {u, static_cast<uint64_t>(M)}, s_act[1] = {u};
-    const uint32_t b_act[2] = {128, kBM};
-    if ((rc = encode(&tm[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.act, d_act, s_act, b_act,
+    const uint64_t d_act[3] = {u, M4, 4}, s_act[2] = {4 * u, u};
+    const uint32_t b_quad[3] = {128, 32, 4};
+    if ((rc = encode(&tm[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, op.act, d_act, s_act, b_quad,
                      CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
       return rc;
-    const uint64_t d_wgt[2] = {u, static_cast<uint64_t>(N)};
-    const uint32_t b_wgt[2] = {128, L::kBNc};
-    if ((rc = encode(&tm[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.wgt, d_wgt, s_act, b_wgt,
+    const uint64_t d_wgt[3] = {u, N4, 4};
+    if ((rc = encode(&tm[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, op.wgt, d_wgt, s_act, b_quad,
                      CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
       return rc;
     const uint64_t d_sfa[2] = {static_cast<uint64_t>(M), static_cast<uint64_t>(K / 16)},
@@ -307,24 +317,23 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
     if ((rc = encode(&tm[3], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.wscales, d_sfb, s_sfb, b_sfb,
                      CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
       return rc;
-    const uint64_t d_out[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)},
-                   s_out[1] = {static_cast<uint64_t>(N) * 2};
-    const uint32_t b_out[2] = {32, 32};
-    if ((rc = encode(&tm[7], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, op.out, d_out, s_out, b_out,
+    // output: one store writes rows 4a + q (a < 32) of a 128-row block
+    const uint64_t d_out[3] = {static_cast<uint64_t>(N), M4, 4},
+                   s_out[2] = {static_cast<uint64_t>(N) * 8, static_cast<uint64_t>(N) * 2};
+    const uint32_t b_out[3] = {32, 32, 1};
+    if ((rc = encode(&tm[7], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, op.out, d_out, s_out, b_out,
                      CU_TENSOR_MAP_SWIZZLE_64B)) != SVDQ_OK)
       return rc;
   }
   if (kp.lora_tma) {
-    const uint64_t d_la[2] = {static_cast<uint64_t>(R), static_cast<uint64_t>(M)},
-                   s_la[1] = {static_cast<uint64_t>(R) * 4};
-    const uint32_t b_la[2] = {kLoraRanks, kBM};
-    if ((rc = encode(&tm[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, op.la, d_la, s_la, b_la,
+    const uint64_t r64 = static_cast<uint64_t>(R);
+    const uint64_t d_la[3] = {r64, M4, 4}, s_la[2] = {16 * r64, 4 * r64};
+    const uint32_t b_lora[3] = {kLoraRanks, 32, 4};
+    if ((rc = encode(&tm[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, op.la, d_la, s_la, b_lora,
                      CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
       return rc;
-    const uint64_t d_lu[2] = {static_cast<uint64_t>(R), static_cast<uint64_t>(N)},
-                   s_lu[1] = {static_cast<uint64_t>(R) * 2};
-    const uint32_t b_lu[2] = {kLoraRanks, L::kBNc};
-    if ((rc = encode(&tm[5], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, op.lu, d_lu, s_lu, b_lu,
+    const uint64_t d_lu[3] = {r64, N4, 4}, s_lu[2] = {8 * r64, 2 * r64};
+    if ((rc = encode(&tm[5], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, op.lu, d_lu, s_lu, b_lora,
                      CU_TENSOR_MAP_SWIZZLE_64B)) != SVDQ_OK)
       return rc;
   } else {

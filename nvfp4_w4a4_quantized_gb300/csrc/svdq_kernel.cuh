@@ -13,13 +13,27 @@
 // 128 output rows; in a pair the leader (cluster rank 0) issues every MMA,
 // A is split along M and B along N between the two CTAs' shared memory.
 //
-// 13 warps per CTA:
-//   warps 0, 12  TMA producers, taking alternate ring items (one issuing
-//                thread streams far fewer bytes per second than two).  Main
-//                ring item (one 256-wide K block): packed act/wgt tiles
-//                (128-byte swizzle) and the raw [16 groups x rows] scale boxes.
-//                LoRA ring item (32 ranks): raw fp32 LA rows, bf16 LU rows
-//                (64-byte swizzle) and wcscale.
+// Row-quad order.  Inside every 128-row block of an operand tile, tile row
+// a + 32b (a < 32, b < 4) holds matrix row 4a + b.  The TMA builds this order
+// itself from a 3-D view of the row-major operand (dims: bytes, row quads,
+// row within the quad).  A and B tiles, the LoRA rows and the output store all
+// use it, so the product is unchanged; what it buys is the scale layout: the
+// tensor-memory word of lane a, column b must hold the four group scales of
+// tile row a + 32b = matrix row 4a + b, and those are four consecutive bytes
+// of each raw [group][row] scale row.  One 32-bit shared load per group and a
+// 4x4 byte transpose in registers give a lane its words: no staging, no
+// exchange between warps.  In tensor memory the accumulator's lanes follow the
+// row order (warp q's lane a is output row 4a + q) and its columns the B order
+// (column 128h + a + 32b is output column 128h + 4a + b).
+//
+// 14 warps per CTA:
+//   warps 0, 12, 13  TMA producers, one thread each, every ring item split
+//                three ways (one issuing thread streams far fewer bytes per
+//                second than three): warp 0 the raw [16 groups x rows] scale
+//                boxes, the LoRA item rows and the leader's byte count; warp 12
+//                the packed act tiles; warp 13 the packed wgt tiles (128-byte
+//                swizzle).  LoRA ring item (32 ranks): raw fp32 LA rows, bf16
+//                LU rows (64-byte swizzle) and wcscale.
 //   warp 1       MMA issuer (one thread, leader CTA): tcgen05.mma kind::mxf4nvf4
 //                block_scale.scale_vec::4X for main items, kind::f16 (bf16) for
 //                LoRA items, commits that free ring stages / publish accumulators.
@@ -27,9 +41,10 @@
 //                written into the stage in the MMA's K-major 64-byte-swizzle layout.
 //   warps 4..7   epilogue: tcgen05.ld -> fma(acc, wc, bias) -> bf16 -> shared
 //                staging (64-byte swizzle) -> TMA tile store.
-//   warps 8..11  scale feeders: relayout the stage's raw M-major scale boxes into
-//                row-per-lane words and write them into tensor memory with
-//                tcgen05.st (one warp per 32-lane quadrant), off the MMA pipe.
+//   warps 8..11  scale feeders: transpose the stage's raw scale boxes into
+//                row-per-lane words in registers and write them into tensor
+//                memory with tcgen05.st (one warp per 32-lane quadrant), off
+//                the MMA pipe.
 // Warp 4+q / 8+q own tensor-memory lanes 32q .. 32q+31.
 //
 // Per output tile the ring carries ceil(R/32) LoRA items, then ceil(K/256)
@@ -53,24 +68,25 @@
 
 namespace svdq {
 
-constexpr int kThreads = 416;
+constexpr int kThreads = 448;
 constexpr int kBM = 128;     // output rows per CTA (per-CTA MMA M)
 constexpr int kBK = 256;     // K elements per K block (128 packed bytes per row)
 constexpr int kLoraRanks = 32;  // ranks per LoRA ring item
 constexpr int kMaxStages = 8;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDrainNs = 200ull * 1000ull * 1000ull;  // teardown drain limit
+// Longest a waiting thread sleeps in one try_wait before it re-checks the
+// abort flag and its time limit.
+constexpr uint32_t kSleepHintNs = 1000u * 1000u;
 
 enum WaitSite : int {
   kSiteProducerEmpty = 1,
   kSiteMmaAccEmpty = 2,
   kSiteMmaFull = 3,
-  kSiteMmaReady = 4,
   kSiteMmaLoraDone = 5,
   kSiteLoraAuxFull = 6,
   kSiteSfAuxFull = 7,
   kSiteEpiAccFull = 8,
-  kSiteSfTranspose = 9,
 };
 
 constexpr int kStatusTimeout = -7;  // == SVDQ_ERR_TIMEOUT
@@ -191,7 +207,8 @@ __device__ __noinline__ void report_timeout(int* status, int site) {
 template <bool CLUSTER>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int site, const Ctl& c) {
   auto probe = [&]() {
-    return CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    return CLUSTER ? ptx::mbar_try_wait_cluster_sleep(bar, parity, kSleepHintNs)
+                   : ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs);
   };
   if (probe()) return true;
   const uint64_t t0 = ptx::globaltimer();
@@ -228,32 +245,31 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
-// In-place relayout of one K-step (4 scale groups) of a raw TMA scale box
-// [4 groups][H*128 rows] into H blocks of 32 rows x 16 bytes: word j of row
-// r of block h holds the 4 group scales (byte g = group g) of row 128h+32j+r.
-template <int H>
-__device__ __forceinline__ void sf_relayout(uint8_t* base, int lane) {
-  uint32_t w[H][4];
-#pragma unroll
-  for (int h = 0; h < H; ++h)
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      w[h][g] = *reinterpret_cast<const uint32_t*>(base + g * (H * 128) + h * 128 + 4 * lane);
-  __syncwarp();
-#pragma unroll
-  for (int h = 0; h < H; ++h) {
-    // 4x4 byte transpose: output i gathers byte i (row 4*lane+i) of groups 0..3.
-    const uint32_t t0 = __byte_perm(w[h][0], w[h][1], 0x5140);
-    const uint32_t t1 = __byte_perm(w[h][0], w[h][1], 0x7362);
-    const uint32_t t2 = __byte_perm(w[h][2], w[h][3], 0x5140);
-    const uint32_t t3 = __byte_perm(w[h][2], w[h][3], 0x7362);
-    uint8_t* dst = base + 512 * h + (lane >> 3) * 4;
-    const int r0 = 4 * (lane & 7);
-    *reinterpret_cast<uint32_t*>(dst + (r0 + 0) * 16) = __byte_perm(t0, t2, 0x5410);
-    *reinterpret_cast<uint32_t*>(dst + (r0 + 1) * 16) = __byte_perm(t0, t2, 0x7632);
-    *reinterpret_cast<uint32_t*>(dst + (r0 + 2) * 16) = __byte_perm(t1, t3, 0x5410);
-    *reinterpret_cast<uint32_t*>(dst + (r0 + 3) * 16) = __byte_perm(t1, t3, 0x7632);
-  }
+// Matrix row (or column) offset held by tile row r under the row-quad order:
+// within each 128-row block, row a + 32b holds offset 4a + b.
+__device__ __forceinline__ int quad_row(int r) {
+  return (r & ~127) | (4 * (r & 31)) | ((r >> 5) & 3);
+}
+
+// Scale words of one K step (4 groups) for one 128-row block.  `raw` points at
+// group 0 of the block in a raw [group][row] scale box with `pitch` bytes per
+// group; lane a gets w[b] = the 4 group scales (byte g = group g) of block row
+// 4a + b, the word tensor-memory lane a, column b takes.
+__device__ __forceinline__ void sf_words(const uint8_t* raw, int pitch, int lane, uint32_t* w) {
+  const uint8_t* p = raw + 4 * lane;
+  const uint32_t g0 = *reinterpret_cast<const uint32_t*>(p);
+  const uint32_t g1 = *reinterpret_cast<const uint32_t*>(p + pitch);
+  const uint32_t g2 = *reinterpret_cast<const uint32_t*>(p + 2 * pitch);
+  const uint32_t g3 = *reinterpret_cast<const uint32_t*>(p + 3 * pitch);
+  // 4x4 byte transpose: byte b of group g -> byte g of word b
+  const uint32_t t0 = __byte_perm(g0, g1, 0x5140);
+  const uint32_t t1 = __byte_perm(g0, g1, 0x7362);
+  const uint32_t t2 = __byte_perm(g2, g3, 0x5140);
+  const uint32_t t3 = __byte_perm(g2, g3, 0x7362);
+  w[0] = __byte_perm(t0, t2, 0x5410);
+  w[1] = __byte_perm(t0, t2, 0x7632);
+  w[2] = __byte_perm(t1, t3, 0x5410);
+  w[3] = __byte_perm(t1, t3, 0x7632);
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..3) of row `row` in a K-major tile
@@ -262,8 +278,9 @@ __device__ __forceinline__ int sw64_offset(int row, int chunk) {
   return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
 }
 
-// LA' from the TMA-staged raw fp32 rows [128][32]: lane reads 4 consecutive
-// floats of a row, writes 4 bf16 (half a 16-byte chunk).
+// LA' from the TMA-staged raw fp32 rows [128][32] (already in row-quad
+// order): lane reads 4 consecutive floats of a row, writes 4 bf16 (half a
+// 16-byte chunk).
 __device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* raw, int lane) {
   const int c = lane & 7;  // 16-byte piece of the 128-byte raw row
 #pragma unroll 4
@@ -277,8 +294,10 @@ __device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* r
   }
 }
 
-// LU' in place: every 16-byte chunk of row n times 1/wcscale[n] (fp32
-// reciprocal and product, bf16 RNE).  Rows outside N (zero-filled) stay zero.
+// LU' in place: every 16-byte chunk of tile row r (column n = n_cta +
+// quad_row(r)) times 1/wcscale[n] (fp32 reciprocal and product, bf16 RNE); the
+// staged wcscale is in plain column order.  Rows outside N (zero-filled) stay
+// zero.
 template <int ROWS>
 __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* wc, int n_cta,
                                                    int N, int lane) {
@@ -286,9 +305,10 @@ __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* w
 #pragma unroll 4
   for (int it = 0; it < ROWS / 8; ++it) {
     const int row = it * 8 + (lane >> 2);
+    const int off = quad_row(row);
     const float w = __uint_as_float(static_cast<uint32_t>(
-                        *reinterpret_cast<const uint16_t*>(wc + 2 * row)) << 16);
-    const float inv = (n_cta + row < N && w != 0.f) ? __frcp_rn(w) : 0.f;
+                        *reinterpret_cast<const uint16_t*>(wc + 2 * off)) << 16);
+    const float inv = (n_cta + off < N && w != 0.f) ? __frcp_rn(w) : 0.f;
     uint4 x = *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc);
     x.x = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.x), inv), __fmul_rn(bf16_hi(x.x), inv));
     x.y = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.y), inv), __fmul_rn(bf16_hi(x.y), inv));
@@ -299,15 +319,16 @@ __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* w
 }
 
 // Direct-load LoRA operands (used when R is not a multiple of 8, so LoRA rows
-// are not 16-byte strided for TMA): LA' rows m_cta.., LU' rows n_cta.., ranks
-// 32*blk .. 32*blk+31, zero outside [M|N, R).
+// are not 16-byte strided for TMA): LA' tile row r holds matrix row m_cta +
+// quad_row(r), LU' tile row r column n_cta + quad_row(r); ranks 32*blk ..
+// 32*blk+31, zero outside [M|N, R).
 __device__ __forceinline__ void lora_la_direct(uint8_t* dst, const KParams& p, int m_cta, int blk,
                                                int lane) {
   const int chunk = lane & 3;
   const int r0 = blk * kLoraRanks + chunk * 8;
   for (int it = 0; it < kBM / 8; ++it) {
     const int row = it * 8 + (lane >> 2);
-    const int m = m_cta + row;
+    const int m = m_cta + quad_row(row);
     float v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -330,7 +351,7 @@ __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p, i
   const uint16_t* wc = reinterpret_cast<const uint16_t*>(p.wcscale);
   for (int it = 0; it < ROWS / 8; ++it) {
     const int row = it * 8 + (lane >> 2);
-    const int n = n_cta + row;
+    const int n = n_cta + quad_row(row);
     float inv = 0.f;
     if (n < p.N) {
       const float w = wc ? __uint_as_float(static_cast<uint32_t>(__ldg(wc + n)) << 16) : 1.f;
@@ -382,8 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
   auto auxfull = [&](int s) { return bar0 + 8u * (2 * kMaxStages + s); };
-  auto ready = [&](int s) { return bar0 + 8u * (3 * kMaxStages + s); };
-  const uint32_t sft = bar0 + 8u * (4 * kMaxStages);
   auto acc_full = [&](int a) { return bar0 + 8u * (5 * kMaxStages + a); };
   auto acc_empty = [&](int a) { return bar0 + 8u * (5 * kMaxStages + 2 + a); };
   const uint32_t lora_done = bar0 + 8u * (5 * kMaxStages + 4);
@@ -398,12 +417,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(full(s), 1);
+      // the leader's count: its scale producer, then the scale feeders and
+      // LoRA builders of every CTA of the group (their shared-memory and
+      // tensor-memory writes are done); the act / wgt bytes come as transactions
+      ptx::mbar_init(full(s), 1 + 6 * CG);
       ptx::mbar_init(empty(s), 1);
-      ptx::mbar_init(auxfull(s), 1);
-      ptx::mbar_init(ready(s), 6 * CG);
+      ptx::mbar_init(auxfull(s), 3);  // one arrival per producer
     }
-    ptx::mbar_init(sft, 4);
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(acc_full(a), 1);
       ptx::mbar_init(acc_empty(a), 4 * CG);
@@ -434,13 +454,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == 0 || warp == 12) {
+  if (warp == 0 || warp >= 12) {
     // ------------------------------------------------------------ producers
     if (lane == 0) {
-      const int who = warp == 0 ? 0 : 1;  // this thread issues ring items j with j % 2 == who
+      // role 0: scale boxes, LoRA rows, the byte counts; 1: act tiles; 2: wgt tiles
+      const int role = warp == 0 ? 0 : warp - 11;
       int stage = 0;
       uint32_t phase = 0;
-      long long j = 0;
       bool ok = true;
       const uint32_t main_aux_bytes = 16 * KBI * (kBM + BN);
       const uint32_t lora_aux_bytes =
@@ -452,43 +472,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m_cta = m0 + kBM * static_cast<int>(rank);
         const int n_cta = n0 + L::kBNc * static_cast<int>(rank);
         const int rot = k_rotation(p, mb, nb);
-        for (int i = 0; i < n_items; ++i, ++j) {
-          if ((j & 1) == who) {
-            if (!wait_bar<false>(empty(stage), phase ^ 1u, kSiteProducerEmpty, ctl)) {
-              ok = false;
-              break;
-            }
-            const uint32_t st = sbase + stage * L::kStageBytes;
-            if (i < p.lora_blocks) {
+        for (int i = 0; i < n_items; ++i) {
+          if (!wait_bar<false>(empty(stage), phase ^ 1u, kSiteProducerEmpty, ctl)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + stage * L::kStageBytes;
+          const uint32_t ab = auxfull(stage);
+          if (role != 0) {
+            // Every producer signs every item on the stage's aux barrier, so no
+            // item is consumed before all three have passed their wait for it:
+            // none can fall two phases behind (or run two ahead) on a barrier
+            // it tracks by parity, LoRA items (no act / wgt loads) included.
+            ptx::mbar_arrive(ab);
+          }
+          if (i < p.lora_blocks) {
+            if (role == 0) {
               if (p.lora_tma) {
-                ptx::mbar_arrive_expect_tx(auxfull(stage), lora_aux_bytes);
-                ptx::tma_load_2d(st + L::kLoraRawLA, &tm_la, auxfull(stage), kLoraRanks * i, m_cta);
-                ptx::tma_load_2d(st + L::kLoraLU, &tm_lu, auxfull(stage), kLoraRanks * i, n_cta);
-                if (p.wcscale != nullptr)
-                  ptx::tma_load_1d(st + L::kLoraWC, &tm_wc, auxfull(stage), n_cta);
+                ptx::mbar_arrive_expect_tx(ab, lora_aux_bytes);
+                ptx::tma_load_3d(st + L::kLoraRawLA, &tm_la, ab, kLoraRanks * i, m_cta / 4, 0);
+#pragma unroll
+                for (int h = 0; h < L::kBNc / 128; ++h)
+                  ptx::tma_load_3d(st + L::kLoraLU + 8192 * h, &tm_lu, ab, kLoraRanks * i,
+                                   (n_cta + 128 * h) / 4, 0);
+                if (p.wcscale != nullptr) ptx::tma_load_1d(st + L::kLoraWC, &tm_wc, ab, n_cta);
               } else {
-                ptx::mbar_arrive(auxfull(stage));
+                ptx::mbar_arrive(ab);
               }
               if (leader) ptx::mbar_arrive(full(stage));
-            } else {
-              const int kb0 = KBI * k_item(p, i - p.lora_blocks, rot);
-              const int nkb = min(KBI, p.k_blocks - kb0);
-              ptx::mbar_arrive_expect_tx(auxfull(stage), main_aux_bytes);
-              ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, auxfull(stage), m_cta, kb0 * 16);
-              ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, auxfull(stage), n0, kb0 * 16);
+            }
+          } else {
+            const int kb0 = KBI * k_item(p, i - p.lora_blocks, rot);
+            const int nkb = min(KBI, p.k_blocks - kb0);
+            if (role == 0) {
+              ptx::mbar_arrive_expect_tx(ab, main_aux_bytes);
+              ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, ab, m_cta, kb0 * 16);
+              ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, ab, n0, kb0 * 16);
+              // The act / wgt loads of this item may land before this count
+              // (the transaction count runs negative meanwhile); the phase
+              // cannot complete before this arrival.
               if (leader)
                 ptx::mbar_arrive_expect_tx(full(stage), CG * nkb * (L::kATile + L::kBTile));
+            } else {
+              const uint32_t fb = to_leader(full(stage));
               for (int kk = 0; kk < nkb; ++kk) {
                 const int kx = (kb0 + kk) * 128;
-                const uint32_t da = st + L::kOffA + kk * L::kATile;
-                const uint32_t db = st + L::kOffB + kk * L::kBTile;
-                if (CG == 2) {
-                  const uint32_t fb = to_leader(full(stage));
-                  ptx::tma_load_2d_pair(da, &tm_act, fb, kx, m_cta);
-                  ptx::tma_load_2d_pair(db, &tm_wgt, fb, kx, n_cta);
+                if (role == 1) {
+                  const uint32_t da = st + L::kOffA + kk * L::kATile;
+                  if (CG == 2)
+                    ptx::tma_load_3d_pair(da, &tm_act, fb, kx, m_cta / 4, 0);
+                  else
+                    ptx::tma_load_3d(da, &tm_act, fb, kx, m_cta / 4, 0);
                 } else {
-                  ptx::tma_load_2d(da, &tm_act, full(stage), kx, m_cta);
-                  ptx::tma_load_2d(db, &tm_wgt, full(stage), kx, n_cta);
+#pragma unroll
+                  for (int h = 0; h < L::kBNc / 128; ++h) {
+                    const uint32_t db = st + L::kOffB + kk * L::kBTile + 16384 * h;
+                    const int y = (n_cta + 128 * h) / 4;
+                    if (CG == 2)
+                      ptx::tma_load_3d_pair(db, &tm_wgt, fb, kx, y, 0);
+                    else
+                      ptx::tma_load_3d(db, &tm_wgt, fb, kx, y, 0);
+                  }
                 }
               }
             }
@@ -519,6 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tile_iter = 0;
       constexpr uint32_t kIdescMain = ptx::idesc_mxf4nvf4(kBM * CG, BN);
       constexpr uint32_t kIdescLora = ptx::idesc_bf16_f32(kBM * CG, BN);
+      const uint64_t desc_a0 = ptx::desc_kmajor_sw128(sbase + L::kOffA);
+      const uint64_t desc_b0 = ptx::desc_kmajor_sw128(sbase + L::kOffB);
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++tile_iter) {
         int mb, nb;
         tile_coords(p, t, mb, nb);
@@ -537,8 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc_stage * BN);
         uint32_t accumulate = 0;
         for (int i = 0; i < n_items; ++i) {
-          if (!wait_bar<CG == 2>(full(stage), phase, kSiteMmaFull, ctl) ||
-              !wait_bar<CG == 2>(ready(stage), phase, kSiteMmaReady, ctl)) {
+          if (!wait_bar<CG == 2>(full(stage), phase, kSiteMmaFull, ctl)) {
             ok = false;
             break;
           }
@@ -577,12 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kb0 = KBI * k_item(p, i - p.lora_blocks, rot);
             const uint32_t sf =
                 tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
-            // K=64 steps present in this item (the last K block may be partial)
-            const int nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
-            for (int ks = 0; ks < nsteps; ++ks) {
-              const int kk = ks >> 2, s = ks & 3;
-              const uint64_t ad = ptx::desc_kmajor_sw128(st + L::kOffA + kk * L::kATile + 32 * s);
-              const uint64_t bd = ptx::desc_kmajor_sw128(st + L::kOffB + kk * L::kBTile + 32 * s);
+            // descriptors of this stage's first K step; a step advances the
+            // start address (descriptor units of 16 bytes)
+            const uint64_t soff = static_cast<uint64_t>((stage * L::kStageBytes) >> 4);
+            const uint64_t ad0 = desc_a0 + soff, bd0 = desc_b0 + soff;
+            auto step = [&](int ks) {
+              const int kk = ks >> 2, s4 = ks & 3;
+              const uint64_t ad = ad0 + static_cast<uint64_t>((kk * L::kATile + 32 * s4) >> 4);
+              const uint64_t bd = bd0 + static_cast<uint64_t>((kk * L::kBTile + 32 * s4) >> 4);
               const uint32_t sfa = sf + 4 * ks;
               const uint32_t sfb = sf + 4 * L::kSteps + 4 * ks * L::kSfbHalves;
               if (CG == 2)
@@ -590,6 +637,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               else
                 ptx::mma_mxf4nvf4(d_tmem, ad, bd, kIdescMain, sfa, sfb, accumulate);
               accumulate = 1;
+            };
+            // K=64 steps present in this item (the last K block may be partial)
+            const int nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
+            if (nsteps == L::kSteps) {
+#pragma unroll
+              for (int ks = 0; ks < L::kSteps; ++ks) step(ks);
+            } else {
+              for (int ks = 0; ks < nsteps; ++ks) step(ks);
             }
             if (CG == 2)
               ptx::mma_commit_pair_multicast(empty(stage), 3);
@@ -619,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ LoRA operand builders
     int stage = 0;
     uint32_t phase = 0;
-    const uint32_t ready_bar0 = to_leader(ready(0));
+    const uint32_t full_bar0 = to_leader(full(0));
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
@@ -651,9 +706,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // The pair peer's LoRA operands are generic shared-memory writes the
           // leader's MMA reads: publish them with a cluster-scope release.
           if (CG == 2 && !leader && i < p.lora_blocks)
-            ptx::mbar_arrive_cluster(ready_bar0 + 8u * stage);
+            ptx::mbar_arrive_cluster(full_bar0 + 8u * stage);
           else
-            ptx::mbar_arrive_remote(ready_bar0 + 8u * stage);
+            ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
         }
         if (++stage == S) {
           stage = 0;
@@ -696,8 +751,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                              static_cast<uint32_t>(acc_stage * BN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(taddr + 32 * c, v);
+        // output columns n0 + 32c + i, i = 4k + b, sit in accumulator column
+        // 128h + 32b + 8(c % 4) + k of this tile (h = c / 4)
+        uint32_t r[4][8];
+        const uint32_t cbase = taddr + 128 * (c >> 2) + 8 * (c & 3);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(cbase + 32 * b, r[b]);
         ptx::tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
@@ -708,9 +767,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bb[4] = {b8.x, b8.y, b8.z, b8.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float y0 = fmaf(__uint_as_float(v[8 * g + 2 * j]), bf16_lo(ww[j]), bf16_lo(bb[j]));
-            const float y1 =
-                fmaf(__uint_as_float(v[8 * g + 2 * j + 1]), bf16_hi(ww[j]), bf16_hi(bb[j]));
+            const int i0 = 8 * g + 2 * j;  // even column of the pair
+            const uint32_t a0 = r[i0 & 3][i0 >> 2], a1 = r[(i0 + 1) & 3][(i0 + 1) >> 2];
+            const float y0 = fmaf(__uint_as_float(a0), bf16_lo(ww[j]), bf16_lo(bb[j]));
+            const float y1 = fmaf(__uint_as_float(a1), bf16_hi(ww[j]), bf16_hi(bb[j]));
             pk[4 * g + j] = ptx::pack_bf16x2(y0, y1);
           }
         }
@@ -725,7 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          ptx::tma_store_2d(&tm_out, ptx::smem_u32(sb), n0 + 32 * c, m_cta + 32 * q);
+          // staging row `lane` is output row m_cta + 4 * lane + q
+          ptx::tma_store_3d(&tm_out, ptx::smem_u32(sb), n0 + 32 * c, m_cta / 4, q);
           ptx::bulk_commit_group();
         }
         buf ^= 1;
@@ -740,8 +801,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ scale feeders
     const int q = warp & 3;
     int stage = 0;
-    uint32_t phase = 0, sft_phase = 0;
-    const uint32_t ready_bar0 = to_leader(ready(0));
+    uint32_t phase = 0;
+    const uint32_t full_bar0 = to_leader(full(0));
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
       bool ok = true;
@@ -751,39 +812,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (i >= p.lora_blocks) {
-          uint8_t* st = smem + stage * L::kStageBytes;
-          // this warp relayouts K steps q, q+4, ... of the stage; the four warps
-          // then share the result
-#pragma unroll
-          for (int ks = q; ks < L::kSteps; ks += 4) {
-            sf_relayout<1>(st + L::kOffSFA + 512 * ks, lane);
-            sf_relayout<L::kSfbHalves>(st + L::kOffSFB + 4 * BN * ks, lane);
-          }
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(sft);
-          if (!warp_wait_bar<false>(sft, sft_phase, kSiteSfTranspose, ctl)) {
-            ok = false;
-            break;
-          }
-          sft_phase ^= 1u;
-          // row (32q + lane) of tensor memory: words j = rows lane + 32j of
-          // each 128-row block, four K steps (one K block) at a time
+          const uint8_t* st = smem + stage * L::kStageBytes;
+          // Every feeder writes the same words into its own lane quadrant:
+          // the block-scaled MMA reads the scale words in every quadrant.
           const uint32_t col = tmem_base + lane_base +
                                static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
 #pragma unroll
           for (int kk = 0; kk < KBI; ++kk) {
             uint32_t a[16], b[16 * L::kSfbHalves];
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              const int ks = 4 * kk + s;
-              const uint4 x = lds128(st + L::kOffSFA + 512 * ks + 16 * lane);
-              a[4 * s] = x.x; a[4 * s + 1] = x.y; a[4 * s + 2] = x.z; a[4 * s + 3] = x.w;
+            for (int s4 = 0; s4 < 4; ++s4) {
+              const int ks = 4 * kk + s4;
+              sf_words(st + L::kOffSFA + 4 * kBM * ks, kBM, lane, a + 4 * s4);
 #pragma unroll
-              for (int h = 0; h < L::kSfbHalves; ++h) {
-                const uint4 y = lds128(st + L::kOffSFB + 4 * BN * ks + 512 * h + 16 * lane);
-                const int o = 4 * (s * L::kSfbHalves + h);
-                b[o] = y.x; b[o + 1] = y.y; b[o + 2] = y.z; b[o + 3] = y.w;
-              }
+              for (int h = 0; h < L::kSfbHalves; ++h)
+                sf_words(st + L::kOffSFB + 4 * BN * ks + 128 * h, BN, lane,
+                         b + 4 * (s4 * L::kSfbHalves + h));
             }
             ptx::tmem_st_32x32b_x16(col + 16 * kk, a);
 #pragma unroll
@@ -795,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_before();
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_remote(ready_bar0 + 8u * stage);
+        if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;

@@ -145,7 +145,7 @@ def test_plan_each_tile_config(lib, cg, tn):
     # per-CTA stage, per K block: A rows 128 x 128 B, B rows (tile_n / cg) x 128 B,
     # raw scale boxes 16 x 128 and 16 x tile_n
     kbi = p["kblocks_per_stage"]
-    assert kbi == (2 if cg == 2 else 1)
+    assert kbi == 1
     assert p["stage_bytes"] == kbi * (128 * 128 + (tn // cg) * 128 + 16 * 128 + 16 * tn)
     assert p["num_ab_stage"] * kbi >= 3
     sf_cols = kbi * 4 * (4 + 4 * (tn // 128))
