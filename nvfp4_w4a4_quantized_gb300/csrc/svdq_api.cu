@@ -320,9 +320,9 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
     // output: one store writes rows 4a + q (a < 32) of a 128-row block
     const uint64_t d_out[3] = {static_cast<uint64_t>(N), M4, 4},
                    s_out[2] = {static_cast<uint64_t>(N) * 8, static_cast<uint64_t>(N) * 2};
-    const uint32_t b_out[3] = {32, 32, 1};
+    const uint32_t b_out[3] = {64, 32, 1};
     if ((rc = encode(&tm[7], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, op.out, d_out, s_out, b_out,
-                     CU_TENSOR_MAP_SWIZZLE_64B)) != SVDQ_OK)
+                     CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
       return rc;
   }
   if (kp.lora_tma) {

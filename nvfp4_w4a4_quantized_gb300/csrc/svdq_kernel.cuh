@@ -39,8 +39,10 @@
 //                LoRA items, commits that free ring stages / publish accumulators.
 //   warps 2, 3   LoRA operand builders: LA' = bf16(LA) and LU' = bf16(LU / wc)
 //                written into the stage in the MMA's K-major 64-byte-swizzle layout.
-//   warps 4..7   epilogue: tcgen05.ld -> fma(acc, wc, bias) -> bf16 -> shared
-//                staging (64-byte swizzle) -> TMA tile store.
+//   warps 4..7   epilogue: tcgen05.ld (64 columns at a time) -> fma(acc, wc, bias)
+//                -> bf16 -> shared staging (128-byte swizzle) -> TMA tile store;
+//                the accumulator is released as soon as its last columns are
+//                in registers.
 //   warps 8..11  scale feeders: transpose the stage's raw scale boxes into
 //                row-per-lane words in registers and write them into tensor
 //                memory with tcgen05.st (one warp per 32-lane quadrant), off
@@ -68,7 +70,7 @@
 
 namespace svdq {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kBM = 128;     // output rows per CTA (per-CTA MMA M)
 constexpr int kBK = 256;     // K elements per K block (128 packed bytes per row)
 constexpr int kLoraRanks = 32;  // ranks per LoRA ring item
@@ -83,7 +85,6 @@ enum WaitSite : int {
   kSiteProducerEmpty = 1,
   kSiteMmaAccEmpty = 2,
   kSiteMmaFull = 3,
-  kSiteMmaLoraDone = 5,
   kSiteLoraAuxFull = 6,
   kSiteSfAuxFull = 7,
   kSiteEpiAccFull = 8,
@@ -125,10 +126,12 @@ struct Layout {
   static constexpr int kAccCols = kAccStages * BN;
   // tensor-memory scale columns per stage: SFA 4 per K step, then SFB 4*halves per K step
   static constexpr int kSfCols = kSteps * (4 + 4 * kSfbHalves);
-  static constexpr int kEpiStageBytes = 32 * 64;        // one 32 x 32 bf16 output tile
-  static constexpr int kEpiBytes = 4 * 2 * kEpiStageBytes;
-  static constexpr int kWcbBytes = 4 * 2 * BN * 2;      // per epilogue warp: wc[BN], bias[BN]
-  static constexpr int kBarCount = 5 * kMaxStages + 6;
+  // epilogue, per warp: one 32 x 64 bf16 staging tile (128-byte rows, 128-byte
+  // swizzle) and the tile's fp32 wcscale[BN], bias[BN]
+  static constexpr int kEpiStageBytes = 32 * 128;
+  static constexpr int kEpiBytes = 4 * kEpiStageBytes;
+  static constexpr int kWcbBytes = 4 * 2 * BN * 4;
+  static constexpr int kBarCount = 5 * kMaxStages + 7;
   static constexpr int kBarBytes = 8 * kBarCount + 16;
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   __host__ __device__ static constexpr int epi_offset(int stages) { return stages * kStageBytes; }
@@ -405,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto auxfull = [&](int s) { return bar0 + 8u * (2 * kMaxStages + s); };
   auto acc_full = [&](int a) { return bar0 + 8u * (5 * kMaxStages + a); };
   auto acc_empty = [&](int a) { return bar0 + 8u * (5 * kMaxStages + 2 + a); };
-  const uint32_t lora_done = bar0 + 8u * (5 * kMaxStages + 4);
-  const uint32_t drain = bar0 + 8u * (5 * kMaxStages + 5);
+  const uint32_t never = bar0 + 8u * (5 * kMaxStages + 4);  // no role arrives on it
+  auto drain = [&](uint32_t e) { return bar0 + 8u * (5 * kMaxStages + 5 + e); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * L::kBarCount);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const Ctl ctl{abort_flag, p.status, p.timeout_ns};
@@ -421,15 +424,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // LoRA builders of every CTA of the group (their shared-memory and
       // tensor-memory writes are done); the act / wgt bytes come as transactions
       ptx::mbar_init(full(s), 1 + 6 * CG);
-      ptx::mbar_init(empty(s), 1);
+      ptx::mbar_init(empty(s), 2);  // the owning issuer's commit, the other's arrival
       ptx::mbar_init(auxfull(s), 3);  // one arrival per producer
     }
     for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(acc_full(a), 1);
-      ptx::mbar_init(acc_empty(a), 4 * CG);
+      ptx::mbar_init(acc_full(a), 2);          // one commit per MMA issuer
+      ptx::mbar_init(acc_empty(a), 4 * CG);    // the epilogue warps of the group
     }
-    ptx::mbar_init(lora_done, 1);
-    ptx::mbar_init(drain, 1);
+    ptx::mbar_init(never, 1);
+    ptx::mbar_init(drain(0), 1);
+    ptx::mbar_init(drain(1), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == 0 || warp >= 12) {
+  if (warp == 0 || warp == 12 || warp == 13) {
     // ------------------------------------------------------------ producers
     if (lane == 0) {
       // role 0: scale boxes, LoRA rows, the byte counts; 1: act tiles; 2: wgt tiles
@@ -554,102 +558,106 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 14) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads of the leader CTA share the ring: issuer e issues the MMAs
+    // of items j with j % 2 == e (j counts items over all tiles), so one
+    // thread's per-item cost (barrier wait, descriptors, commit) is spread
+    // over two items' worth of tensor-core time.  Both wait on every item's
+    // full barrier in order and signs every item's release, so neither can
+    // fall two phases behind on a barrier it tracks by parity.
+    // Every MMA accumulates: the epilogue zeroes the accumulator when it has
+    // read it (and once before the first tile), so the order in which the
+    // two issuers' MMAs reach the tensor core does not matter.
     if (lane == 0 && leader) {
+      const uint32_t me = warp == 1 ? 0u : 1u;
       int stage = 0;
-      uint32_t phase = 0, lora_phase = 0;
+      uint32_t phase = 0;
+      uint32_t j = 0;
       bool ok = true;
       int tile_iter = 0;
       constexpr uint32_t kIdescMain = ptx::idesc_mxf4nvf4(kBM * CG, BN);
       constexpr uint32_t kIdescLora = ptx::idesc_bf16_f32(kBM * CG, BN);
       const uint64_t desc_a0 = ptx::desc_kmajor_sw128(sbase + L::kOffA);
       const uint64_t desc_b0 = ptx::desc_kmajor_sw128(sbase + L::kOffB);
+      const bool k_ragged = (p.K % kBK) != 0;  // the last K block is partial
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++tile_iter) {
         int mb, nb;
         tile_coords(p, t, mb, nb);
         const int rot = k_rotation(p, mb, nb);
         const int acc_stage = tile_iter % L::kAccStages;
         const uint32_t acc_phase = static_cast<uint32_t>(tile_iter / L::kAccStages) & 1u;
-        // A free accumulator: the epilogue released this buffer's previous tile.
-        // (debug_fault inverts the expected phase -- the single-stage
-        // "producer must start at phase 1" mistake -- so the wait expires.)
-        if (!wait_bar<CG == 2>(acc_empty(acc_stage), acc_phase ^ 1u ^ (p.debug_fault ? 1u : 0u),
-                          kSiteMmaAccEmpty, ctl)) {
+        // A zeroed accumulator: the epilogue read this buffer's previous tile
+        // (or cleared it at start).  debug_fault waits on a barrier no role
+        // arrives on instead, so the wait must expire.
+        const bool got = p.debug_fault ? wait_bar<false>(never, 0u, kSiteMmaAccEmpty, ctl)
+                                       : wait_bar<CG == 2>(acc_empty(acc_stage), acc_phase,
+                                                           kSiteMmaAccEmpty, ctl);
+        if (!got) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc_stage * BN);
-        uint32_t accumulate = 0;
-        for (int i = 0; i < n_items; ++i) {
+        for (int i = 0; i < n_items; ++i, ++j) {
           if (!wait_bar<CG == 2>(full(stage), phase, kSiteMmaFull, ctl)) {
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
-          const uint32_t st = sbase + stage * L::kStageBytes;
-          if (i < p.lora_blocks) {
-            const int nsteps = min(2, (p.r16 - kLoraRanks * i) / 16);
-            for (int s = 0; s < nsteps; ++s) {
-              const uint64_t ad = ptx::desc_kmajor_sw64(st + L::kLoraLA + 32 * s);
-              const uint64_t bd = ptx::desc_kmajor_sw64(st + L::kLoraLU + 32 * s);
-              if (CG == 2)
-                ptx::mma_bf16_pair(d_tmem, ad, bd, kIdescLora, accumulate);
-              else
-                ptx::mma_bf16(d_tmem, ad, bd, kIdescLora, accumulate);
-              accumulate = 1;
-            }
-            if (CG == 2)
-              ptx::mma_commit_pair_multicast(empty(stage), 3);
-            else
-              ptx::mma_commit(empty(stage));
-            if (i == p.lora_blocks - 1) {
-              // Different MMA kinds on one accumulator: let the LoRA products
-              // land before the first block-scaled MMA reads the accumulator.
-              if (CG == 2)
-                ptx::mma_commit_pair(lora_done);
-              else
-                ptx::mma_commit(lora_done);
-              if (!wait_bar<false>(lora_done, lora_phase, kSiteMmaLoraDone, ctl)) {
-                ok = false;
-                break;
+          if ((j & 1u) == me) {
+            ptx::tc_fence_after();
+            const uint32_t st = sbase + stage * L::kStageBytes;
+            if (i < p.lora_blocks) {
+              const int nsteps = min(2, (p.r16 - kLoraRanks * i) / 16);
+              for (int s = 0; s < nsteps; ++s) {
+                const uint64_t ad = ptx::desc_kmajor_sw64(st + L::kLoraLA + 32 * s);
+                const uint64_t bd = ptx::desc_kmajor_sw64(st + L::kLoraLU + 32 * s);
+                if (CG == 2)
+                  ptx::mma_bf16_pair(d_tmem, ad, bd, kIdescLora, 1u);
+                else
+                  ptx::mma_bf16(d_tmem, ad, bd, kIdescLora, 1u);
               }
-              lora_phase ^= 1u;
-              ptx::tc_fence_after();
-            }
-          } else {
-            const int kb0 = KBI * k_item(p, i - p.lora_blocks, rot);
-            const uint32_t sf =
-                tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
-            // descriptors of this stage's first K step; a step advances the
-            // start address (descriptor units of 16 bytes)
-            const uint64_t soff = static_cast<uint64_t>((stage * L::kStageBytes) >> 4);
-            const uint64_t ad0 = desc_a0 + soff, bd0 = desc_b0 + soff;
-            auto step = [&](int ks) {
-              const int kk = ks >> 2, s4 = ks & 3;
-              const uint64_t ad = ad0 + static_cast<uint64_t>((kk * L::kATile + 32 * s4) >> 4);
-              const uint64_t bd = bd0 + static_cast<uint64_t>((kk * L::kBTile + 32 * s4) >> 4);
-              const uint32_t sfa = sf + 4 * ks;
-              const uint32_t sfb = sf + 4 * L::kSteps + 4 * ks * L::kSfbHalves;
-              if (CG == 2)
-                ptx::mma_mxf4nvf4_pair(d_tmem, ad, bd, kIdescMain, sfa, sfb, accumulate);
-              else
-                ptx::mma_mxf4nvf4(d_tmem, ad, bd, kIdescMain, sfa, sfb, accumulate);
-              accumulate = 1;
-            };
-            // K=64 steps present in this item (the last K block may be partial)
-            const int nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
-            if (nsteps == L::kSteps) {
-#pragma unroll
-              for (int ks = 0; ks < L::kSteps; ++ks) step(ks);
             } else {
-              for (int ks = 0; ks < nsteps; ++ks) step(ks);
+              const uint32_t sf =
+                  tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
+              // descriptors of this stage's first K step; a step advances the
+              // start address (descriptor units of 16 bytes)
+              const uint64_t soff = static_cast<uint64_t>((stage * L::kStageBytes) >> 4);
+              const uint64_t ad0 = desc_a0 + soff, bd0 = desc_b0 + soff;
+              auto step = [&](int ks) {
+                const int kk = ks >> 2, s4 = ks & 3;
+                const uint64_t ad = ad0 + static_cast<uint64_t>((kk * L::kATile + 32 * s4) >> 4);
+                const uint64_t bd = bd0 + static_cast<uint64_t>((kk * L::kBTile + 32 * s4) >> 4);
+                const uint32_t sfa = sf + 4 * ks;
+                const uint32_t sfb = sf + 4 * L::kSteps + 4 * ks * L::kSfbHalves;
+                if (CG == 2)
+                  ptx::mma_mxf4nvf4_pair(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
+                else
+                  ptx::mma_mxf4nvf4(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
+              };
+              // K=64 steps present in this item (the last K block may be partial)
+              int nsteps = L::kSteps;
+              if (k_ragged) {
+                const int kb0 = KBI * k_item(p, i - p.lora_blocks, rot);
+                nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
+              }
+              if (nsteps == L::kSteps) {
+#pragma unroll
+                for (int ks = 0; ks < L::kSteps; ++ks) step(ks);
+              } else {
+                for (int ks = 0; ks < nsteps; ++ks) step(ks);
+              }
             }
             if (CG == 2)
               ptx::mma_commit_pair_multicast(empty(stage), 3);
             else
               ptx::mma_commit(empty(stage));
+          } else {
+            // Not this issuer's item: sign the stage's release anyway, so the
+            // producers refill it only after both issuers have passed its
+            // full barrier (neither can then be lapped on that barrier).
+            ptx::mbar_arrive(empty(stage));
+            if (CG == 2) ptx::mbar_arrive_remote(ptx::mapa(empty(stage), 1));
           }
           if (++stage == S) {
             stage = 0;
@@ -657,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
+        // this issuer's share of the tile is done (the epilogue waits for both)
         if (CG == 2)
           ptx::mma_commit_pair_multicast(acc_full(acc_stage), 3);
         else
@@ -664,10 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every tcgen05 operation issued here completes before tensor memory is freed.
       if (CG == 2)
-        ptx::mma_commit_pair(drain);
+        ptx::mma_commit_pair(drain(me));
       else
-        ptx::mma_commit(drain);
-      drain_wait(drain, 0);
+        ptx::mma_commit(drain(me));
+      drain_wait(drain(me), 0);
     }
     __syncwarp();
   } else if (warp < 4) {
@@ -722,78 +731,106 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // tensor-memory lane quadrant of this warp
     const uint16_t* wcg = reinterpret_cast<const uint16_t*>(p.wcscale);
     const uint16_t* big = reinterpret_cast<const uint16_t*>(p.bias);
-    uint8_t* wcb = smem + L::wcb_offset(S) + q * (4 * BN);  // wc[BN] then bias[BN], bf16
-    uint8_t* stg = smem + L::epi_offset(S) + q * (2 * L::kEpiStageBytes);
+    uint8_t* stg = smem + L::epi_offset(S) + q * L::kEpiStageBytes;
+    float* wb = reinterpret_cast<float*>(smem + L::wcb_offset(S) + q * (8 * BN));  // wc, bias
     const uint32_t acc_empty0 = to_leader(acc_empty(0));
-    int tile_iter = 0, buf = 0;
+    const uint32_t zero8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    const uint32_t lane_q = static_cast<uint32_t>(32 * q) << 16;
+    // The MMAs only accumulate: clear every accumulator buffer once before the
+    // first tile (each warp its own 32 lanes), then hand them to the MMA issuers.
+    for (int a = 0; a < L::kAccStages; ++a)
+      for (int c = 0; c < BN; c += 8)
+        ptx::tmem_st_32x32b_x8(tmem_base + lane_q + static_cast<uint32_t>(a * BN + c), zero8);
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0)
+      for (int a = 0; a < L::kAccStages; ++a) ptx::mbar_arrive_remote(acc_empty0 + 8u * a);
+    int tile_iter = 0;
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++tile_iter) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
       const int n0 = nb * BN;
-      // this tile's wcscale / bias (8 columns per lane) while the accumulator fills
-      uint4 wv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // 1.0
-      uint4 bv = make_uint4(0u, 0u, 0u, 0u);
-      if (lane < BN / 8 && n0 + 8 * lane < p.N) {
-        if (wcg) wv = __ldg(reinterpret_cast<const uint4*>(wcg + n0 + 8 * lane));
-        if (big) bv = __ldg(reinterpret_cast<const uint4*>(big + n0 + 8 * lane));
+      // This tile's wcscale / bias as fp32 in this warp's own buffer (no other
+      // warp reads it; the previous tile's reads are behind us in program order).
+      if (lane < BN / 8) {
+        const int c = 8 * lane;
+        uint4 wv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // 1.0
+        uint4 bv = make_uint4(0u, 0u, 0u, 0u);
+        if (n0 + c < p.N) {
+          if (wcg) wv = __ldg(reinterpret_cast<const uint4*>(wcg + n0 + c));
+          if (big) bv = __ldg(reinterpret_cast<const uint4*>(big + n0 + c));
+        }
+        const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          *reinterpret_cast<float4*>(wb + c + 4 * i) =
+              make_float4(bf16_lo(w4[2 * i]), bf16_hi(w4[2 * i]), bf16_lo(w4[2 * i + 1]),
+                          bf16_hi(w4[2 * i + 1]));
+          *reinterpret_cast<float4*>(wb + BN + c + 4 * i) =
+              make_float4(bf16_lo(b4[2 * i]), bf16_hi(b4[2 * i]), bf16_lo(b4[2 * i + 1]),
+                          bf16_hi(b4[2 * i + 1]));
+        }
       }
+      __syncwarp();
       const int acc_stage = tile_iter % L::kAccStages;
       const uint32_t acc_phase = static_cast<uint32_t>(tile_iter / L::kAccStages) & 1u;
       if (!warp_wait_bar<false>(acc_full(acc_stage), acc_phase, kSiteEpiAccFull, ctl)) break;
       ptx::tc_fence_after();
-      if (lane < BN / 8) {
-        *reinterpret_cast<uint4*>(wcb + 16 * lane) = wv;
-        *reinterpret_cast<uint4*>(wcb + 2 * BN + 16 * lane) = bv;
-      }
-      __syncwarp();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc_stage * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        // output columns n0 + 32c + i, i = 4k + b, sit in accumulator column
-        // 128h + 32b + 8(c % 4) + k of this tile (h = c / 4)
-        uint32_t r[4][8];
-        const uint32_t cbase = taddr + 128 * (c >> 2) + 8 * (c & 3);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(cbase + 32 * b, r[b]);
-        ptx::tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint4 w8 = lds128(wcb + 2 * (32 * c + 8 * g));
-          const uint4 b8 = lds128(wcb + 2 * BN + 2 * (32 * c + 8 * g));
-          const uint32_t ww[4] = {w8.x, w8.y, w8.z, w8.w};
-          const uint32_t bb[4] = {b8.x, b8.y, b8.z, b8.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int i0 = 8 * g + 2 * j;  // even column of the pair
-            const uint32_t a0 = r[i0 & 3][i0 >> 2], a1 = r[(i0 + 1) & 3][(i0 + 1) >> 2];
-            const float y0 = fmaf(__uint_as_float(a0), bf16_lo(ww[j]), bf16_lo(bb[j]));
-            const float y1 = fmaf(__uint_as_float(a1), bf16_hi(ww[j]), bf16_hi(bb[j]));
-            pk[4 * g + j] = ptx::pack_bf16x2(y0, y1);
-          }
-        }
-        // staging buffer `buf` must no longer be read by its previous store
-        if (lane == 0) ptx::bulk_wait_group_read<1>();
+      for (int c2 = 0; c2 < BN / 64; ++c2) {
+        // Output columns n0 + 64 c2 + 32 u + 4k + b (u < 2, b < 4, k < 8) sit
+        // in accumulator column 128h + 32b + 8(2 c2 % 4 + u) + k, h = c2 / 2.
+        const uint32_t cbase = taddr + 128 * (c2 >> 1) + 16 * (c2 & 1);
+        // the staging tile must no longer be read by its previous store
+        if (lane == 0) ptx::bulk_wait_group_read<0>();
         __syncwarp();
-        uint8_t* sb = stg + buf * L::kEpiStageBytes;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(sb + sw64_offset(lane, j)) =
-              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        for (int u = 0; u < 2; ++u) {
+          uint32_t r[4][8];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(cbase + 8 * u + 32 * b, r[b]);
+          ptx::tmem_wait_ld();
+          // read: clear these columns for the next tile's accumulation
+#pragma unroll
+          for (int b = 0; b < 4; ++b) ptx::tmem_st_32x32b_x8(cbase + 8 * u + 32 * b, zero8);
+          if (c2 == BN / 64 - 1 && u == 1) {
+            // the whole accumulator is read and cleared: release it to the MMA
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int o = 64 * c2 + 32 * u + 4 * k;
+            const float4 w = *reinterpret_cast<const float4*>(wb + o);
+            const float4 bb = *reinterpret_cast<const float4*>(wb + BN + o);
+            const float y0 = fmaf(__uint_as_float(r[0][k]), w.x, bb.x);
+            const float y1 = fmaf(__uint_as_float(r[1][k]), w.y, bb.y);
+            const float y2 = fmaf(__uint_as_float(r[2][k]), w.z, bb.z);
+            const float y3 = fmaf(__uint_as_float(r[3][k]), w.w, bb.w);
+            pk[2 * k] = ptx::pack_bf16x2(y0, y1);
+            pk[2 * k + 1] = ptx::pack_bf16x2(y2, y3);
+          }
+          // 16-byte chunk j of the 128-byte row holds columns 8j .. 8j+7
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(stg + 128 * lane + (((4 * u + j) ^ (lane & 7)) << 4)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           // staging row `lane` is output row m_cta + 4 * lane + q
-          ptx::tma_store_3d(&tm_out, ptx::smem_u32(sb), n0 + 32 * c, m_cta / 4, q);
+          ptx::tma_store_3d(&tm_out, ptx::smem_u32(stg), n0 + 64 * c2, m_cta / 4, q);
           ptx::bulk_commit_group();
         }
-        buf ^= 1;
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
     }
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();
