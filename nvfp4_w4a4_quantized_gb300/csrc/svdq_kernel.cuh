@@ -866,11 +866,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sf_words(st + L::kOffSFB + 4 * BN * ks + 128 * h, BN, lane,
                          b + 4 * (s4 * L::kSfbHalves + h));
             }
-            ptx::tmem_st_32x32b_x16(col + 16 * kk, a);
+            if (KBI == 1 && L::kSfbHalves == 2) {
+              // one K block: SFA (16 columns) and SFB (32) are adjacent; two
+              // stores instead of three (each store briefly holds up the MMAs)
+              uint32_t v[32];
 #pragma unroll
-            for (int h = 0; h < L::kSfbHalves; ++h)
-              ptx::tmem_st_32x32b_x16(col + 4 * L::kSteps + 16 * L::kSfbHalves * kk + 16 * h,
-                                      b + 16 * h);
+              for (int x = 0; x < 16; ++x) {
+                v[x] = a[x];
+                v[16 + x] = b[x];
+              }
+              ptx::tmem_st_32x32b_x32(col, v);
+              ptx::tmem_st_32x32b_x16(col + 32, b + 16);
+            } else {
+              ptx::tmem_st_32x32b_x16(col + 16 * kk, a);
+#pragma unroll
+              for (int h = 0; h < L::kSfbHalves; ++h)
+                ptx::tmem_st_32x32b_x16(col + 4 * L::kSteps + 16 * L::kSfbHalves * kk + 16 * h,
+                                        b + 16 * h);
+            }
           }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
