@@ -277,13 +277,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
-// Arrive with cluster-scope release: publishes this thread's generic
-// shared-memory writes to the other CTA of the pair.  Markedly slower (the
-// release stalls the issuing warp), so used only where that is needed.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
-}
 // Bounded-wait building block with cluster-scope acquire (remote arrivals).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;

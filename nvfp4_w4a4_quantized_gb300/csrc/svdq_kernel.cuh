@@ -37,8 +37,9 @@
 //   warp 1       MMA issuer (one thread, leader CTA): tcgen05.mma kind::mxf4nvf4
 //                block_scale.scale_vec::4X for main items, kind::f16 (bf16) for
 //                LoRA items, commits that free ring stages / publish accumulators.
-//   warps 2, 3   LoRA operand builders: LA' = bf16(LA) and LU' = bf16(LU / wc)
-//                written into the stage in the MMA's K-major 64-byte-swizzle layout.
+//   warps 2, 3   LoRA operand builders: LU' = bf16(LU / wc), half the rows each,
+//                written into the stage in the MMA's K-major 64-byte-swizzle layout
+//                (the scale feeders build LA' = bf16(LA), 32 rows each).
 //   warps 4..7   epilogue: tcgen05.ld (64 columns at a time) -> fma(acc, wc, bias)
 //                -> bf16 -> shared staging (128-byte swizzle) -> TMA tile store;
 //                the accumulator is released as soon as its last columns are
@@ -281,14 +282,15 @@ __device__ __forceinline__ int sw64_offset(int row, int chunk) {
   return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
 }
 
-// LA' from the TMA-staged raw fp32 rows [128][32] (already in row-quad
-// order): lane reads 4 consecutive floats of a row, writes 4 bf16 (half a
-// 16-byte chunk).
-__device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* raw, int lane) {
+// LA' rows r0 .. r0+31 from the TMA-staged raw fp32 rows [128][32] (already in
+// row-quad order): lane reads 4 consecutive floats of a row, writes 4 bf16
+// (half a 16-byte chunk).
+__device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* raw, int r0,
+                                                  int lane) {
   const int c = lane & 7;  // 16-byte piece of the 128-byte raw row
-#pragma unroll 4
-  for (int it = 0; it < kBM / 4; ++it) {
-    const int row = it * 4 + (lane >> 3);
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int row = r0 + it * 4 + (lane >> 3);
     const float4 v = *reinterpret_cast<const float4*>(raw + row * 128 + 16 * c);
     uint2 pk;
     pk.x = ptx::pack_bf16x2(v.x, v.y);
@@ -297,26 +299,40 @@ __device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* r
   }
 }
 
-// LU' in place: every 16-byte chunk of tile row r (column n = n_cta +
-// quad_row(r)) times 1/wcscale[n] (fp32 reciprocal and product, bf16 RNE); the
-// staged wcscale is in plain column order.  Rows outside N (zero-filled) stay
-// zero.
-template <int ROWS>
-__device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* wc, int n_cta,
-                                                   int N, int lane) {
-  const int pc = lane & 3;
-#pragma unroll 4
-  for (int it = 0; it < ROWS / 8; ++it) {
-    const int row = it * 8 + (lane >> 2);
-    const int off = quad_row(row);
+// 1/wcscale for tile rows r0 + lane + 32t (t < NR/32), 0 outside N or for a
+// zero wcscale (fp32 reciprocal, correctly rounded).
+template <int NR>
+__device__ __forceinline__ void lora_inv_wc(float* inv, const uint8_t* wc, int n_cta, int N,
+                                            int r0, int lane) {
+#pragma unroll
+  for (int t = 0; t < NR / 32; ++t) {
+    const int off = quad_row(r0 + lane + 32 * t);
     const float w = __uint_as_float(static_cast<uint32_t>(
                         *reinterpret_cast<const uint16_t*>(wc + 2 * off)) << 16);
-    const float inv = (n_cta + off < N && w != 0.f) ? __frcp_rn(w) : 0.f;
+    inv[t] = (n_cta + off < N && w != 0.f) ? __frcp_rn(w) : 0.f;
+  }
+}
+
+// LU' rows r0 .. r0+NR-1 in place: every 16-byte chunk of tile row r (column
+// n = n_cta + quad_row(r)) times 1/wcscale[n] (fp32 product, bf16 RNE); the
+// staged wcscale is in plain column order.  Rows outside N (zero-filled) stay
+// zero.  Each row's reciprocal is computed once and shuffled to the row's
+// four lanes.
+template <int NR>
+__device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* wc, int n_cta,
+                                                   int N, int r0, int lane) {
+  float inv[NR / 32];
+  lora_inv_wc<NR>(inv, wc, n_cta, N, r0, lane);
+  const int pc = lane & 3;
+#pragma unroll
+  for (int it = 0; it < NR / 8; ++it) {
+    const int row = r0 + it * 8 + (lane >> 2);
+    const float s = __shfl_sync(0xffffffffu, inv[it / 4], (it % 4) * 8 + (lane >> 2));
     uint4 x = *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc);
-    x.x = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.x), inv), __fmul_rn(bf16_hi(x.x), inv));
-    x.y = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.y), inv), __fmul_rn(bf16_hi(x.y), inv));
-    x.z = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.z), inv), __fmul_rn(bf16_hi(x.z), inv));
-    x.w = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.w), inv), __fmul_rn(bf16_hi(x.w), inv));
+    x.x = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.x), s), __fmul_rn(bf16_hi(x.x), s));
+    x.y = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.y), s), __fmul_rn(bf16_hi(x.y), s));
+    x.z = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.z), s), __fmul_rn(bf16_hi(x.z), s));
+    x.w = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.w), s), __fmul_rn(bf16_hi(x.w), s));
     *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc) = x;
   }
 }
@@ -324,18 +340,19 @@ __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* w
 // Direct-load LoRA operands (used when R is not a multiple of 8, so LoRA rows
 // are not 16-byte strided for TMA): LA' tile row r holds matrix row m_cta +
 // quad_row(r), LU' tile row r column n_cta + quad_row(r); ranks 32*blk ..
-// 32*blk+31, zero outside [M|N, R).
+// 32*blk+31, zero outside [M|N, R).  Rows r0 .. r0+NR-1.
+template <int NR>
 __device__ __forceinline__ void lora_la_direct(uint8_t* dst, const KParams& p, int m_cta, int blk,
-                                               int lane) {
+                                               int r0, int lane) {
   const int chunk = lane & 3;
-  const int r0 = blk * kLoraRanks + chunk * 8;
-  for (int it = 0; it < kBM / 8; ++it) {
-    const int row = it * 8 + (lane >> 2);
+  const int k0 = blk * kLoraRanks + chunk * 8;
+  for (int it = 0; it < NR / 8; ++it) {
+    const int row = r0 + it * 8 + (lane >> 2);
     const int m = m_cta + quad_row(row);
     float v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
-      v[q] = (m < p.M && r0 + q < p.R) ? __ldg(p.lora_act_in + (size_t)m * p.R + r0 + q) : 0.f;
+      v[q] = (m < p.M && k0 + q < p.R) ? __ldg(p.lora_act_in + (size_t)m * p.R + k0 + q) : 0.f;
     uint4 pk;
     pk.x = ptx::pack_bf16x2(v[0], v[1]);
     pk.y = ptx::pack_bf16x2(v[2], v[3]);
@@ -345,15 +362,15 @@ __device__ __forceinline__ void lora_la_direct(uint8_t* dst, const KParams& p, i
   }
 }
 
-template <int ROWS>
+template <int NR>
 __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p, int n_cta, int blk,
-                                               int lane) {
+                                               int r0, int lane) {
   const int chunk = lane & 3;
-  const int r0 = blk * kLoraRanks + chunk * 8;
+  const int k0 = blk * kLoraRanks + chunk * 8;
   const uint16_t* lu = reinterpret_cast<const uint16_t*>(p.lora_up);
   const uint16_t* wc = reinterpret_cast<const uint16_t*>(p.wcscale);
-  for (int it = 0; it < ROWS / 8; ++it) {
-    const int row = it * 8 + (lane >> 2);
+  for (int it = 0; it < NR / 8; ++it) {
+    const int row = r0 + it * 8 + (lane >> 2);
     const int n = n_cta + quad_row(row);
     float inv = 0.f;
     if (n < p.N) {
@@ -363,9 +380,9 @@ __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p, i
     float v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
-      v[q] = (n < p.N && r0 + q < p.R)
+      v[q] = (n < p.N && k0 + q < p.R)
                  ? __fmul_rn(__uint_as_float(static_cast<uint32_t>(
-                                 __ldg(lu + (size_t)n * p.R + r0 + q)) << 16),
+                                 __ldg(lu + (size_t)n * p.R + k0 + q)) << 16),
                              inv)
                  : 0.f;
     uint4 pk;
@@ -687,7 +704,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
-      const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
       const int n_cta = nb * BN + L::kBNc * static_cast<int>(rank);
       bool ok = true;
       for (int i = 0; i < n_items; ++i) {
@@ -696,29 +712,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (i < p.lora_blocks) {
+          // LU' rows [h kBNc/2, (h+1) kBNc/2) (the scale feeders build LA')
           uint8_t* st = smem + stage * L::kStageBytes;
-          if (warp == 2) {
-            if (p.lora_tma)
-              lora_la_from_smem(st + L::kLoraLA, st + L::kLoraRawLA, lane);
-            else
-              lora_la_direct(st + L::kLoraLA, p, m_cta, i, lane);
-          } else {
-            if (!p.lora_tma)
-              lora_lu_direct<L::kBNc>(st + L::kLoraLU, p, n_cta, i, lane);
-            else if (p.wcscale != nullptr)
-              lora_lu_scale_smem<L::kBNc>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, lane);
-          }
+          const int r0 = (warp - 2) * (L::kBNc / 2);
+          if (!p.lora_tma)
+            lora_lu_direct<L::kBNc / 2>(st + L::kLoraLU, p, n_cta, i, r0, lane);
+          else if (p.wcscale != nullptr)
+            lora_lu_scale_smem<L::kBNc / 2>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, r0,
+                                            lane);
           ptx::fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) {
-          // The pair peer's LoRA operands are generic shared-memory writes the
-          // leader's MMA reads: publish them with a cluster-scope release.
-          if (CG == 2 && !leader && i < p.lora_blocks)
-            ptx::mbar_arrive_cluster(full_bar0 + 8u * stage);
-          else
-            ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
-        }
+        // The pair peer's LoRA rows are generic shared-memory writes that the
+        // leader's MMA reads: the proxy fence above orders them before this
+        // arrival (CTA-scope release, as for every other arrival here).
+        if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
@@ -780,55 +788,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc_stage * BN);
-#pragma unroll 1
-      for (int c2 = 0; c2 < BN / 64; ++c2) {
-        // Output columns n0 + 64 c2 + 32 u + 4k + b (u < 2, b < 4, k < 8) sit
-        // in accumulator column 128h + 32b + 8(2 c2 % 4 + u) + k, h = c2 / 2.
-        const uint32_t cbase = taddr + 128 * (c2 >> 1) + 16 * (c2 & 1);
-        // the staging tile must no longer be read by its previous store
-        if (lane == 0) ptx::bulk_wait_group_read<0>();
-        __syncwarp();
+      // Column group g (32 output columns n0 + 32g + 4k + b, k < 8, b < 4) sits in
+      // accumulator columns 128h + 32b + 8(g % 4) + k, h = g / 4.  Groups are
+      // software-pipelined: group g+1's tensor-memory loads are in flight while
+      // group g is scaled, converted and staged; two groups make one 64-column
+      // TMA store.
+      constexpr int kGroups = BN / 32;
+      auto gcol = [&](int g) { return taddr + 128 * (g >> 2) + 8 * (g & 3); };
+      uint32_t ra[4][8], rb[4][8];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          uint32_t r[4][8];
+      for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(0) + 32 * b, ra[b]);
+      ptx::tmem_wait_ld();
 #pragma unroll
-          for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(cbase + 8 * u + 32 * b, r[b]);
-          ptx::tmem_wait_ld();
-          // read: clear these columns for the next tile's accumulation
+      for (int g = 0; g < kGroups; ++g) {
+        uint32_t(&cur)[4][8] = (g & 1) ? rb : ra;
+        uint32_t(&nxt)[4][8] = (g & 1) ? ra : rb;
+        // read: clear these columns for the next tile's accumulation
 #pragma unroll
-          for (int b = 0; b < 4; ++b) ptx::tmem_st_32x32b_x8(cbase + 8 * u + 32 * b, zero8);
-          if (c2 == BN / 64 - 1 && u == 1) {
-            // the whole accumulator is read and cleared: release it to the MMA
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
-          }
-          uint32_t pk[16];
+        for (int b = 0; b < 4; ++b) ptx::tmem_st_32x32b_x8(gcol(g) + 32 * b, zero8);
+        if (g + 1 < kGroups) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int o = 64 * c2 + 32 * u + 4 * k;
-            const float4 w = *reinterpret_cast<const float4*>(wb + o);
-            const float4 bb = *reinterpret_cast<const float4*>(wb + BN + o);
-            const float y0 = fmaf(__uint_as_float(r[0][k]), w.x, bb.x);
-            const float y1 = fmaf(__uint_as_float(r[1][k]), w.y, bb.y);
-            const float y2 = fmaf(__uint_as_float(r[2][k]), w.z, bb.z);
-            const float y3 = fmaf(__uint_as_float(r[3][k]), w.w, bb.w);
-            pk[2 * k] = ptx::pack_bf16x2(y0, y1);
-            pk[2 * k + 1] = ptx::pack_bf16x2(y2, y3);
-          }
-          // 16-byte chunk j of the 128-byte row holds columns 8j .. 8j+7
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(stg + 128 * lane + (((4 * u + j) ^ (lane & 7)) << 4)) =
-                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(g + 1) + 32 * b, nxt[b]);
         }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          // staging row `lane` is output row m_cta + 4 * lane + q
-          ptx::tma_store_3d(&tm_out, ptx::smem_u32(stg), n0 + 64 * c2, m_cta / 4, q);
-          ptx::bulk_commit_group();
+        if ((g & 1) == 0) {
+          // the staging tile must no longer be read by its previous store
+          if (lane == 0) ptx::bulk_wait_group_read<0>();
+          __syncwarp();
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int o = 32 * g + 4 * k;
+          const float4 w = *reinterpret_cast<const float4*>(wb + o);
+          const float4 bb = *reinterpret_cast<const float4*>(wb + BN + o);
+          const float y0 = fmaf(__uint_as_float(cur[0][k]), w.x, bb.x);
+          const float y1 = fmaf(__uint_as_float(cur[1][k]), w.y, bb.y);
+          const float y2 = fmaf(__uint_as_float(cur[2][k]), w.z, bb.z);
+          const float y3 = fmaf(__uint_as_float(cur[3][k]), w.w, bb.w);
+          pk[2 * k] = ptx::pack_bf16x2(y0, y1);
+          pk[2 * k + 1] = ptx::pack_bf16x2(y2, y3);
+        }
+        // 16-byte chunk j of the 128-byte staging row holds columns 8j .. 8j+7
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(stg + 128 * lane + (((4 * (g & 1) + j) ^ (lane & 7)) << 4)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        if (g + 1 < kGroups) {
+          ptx::tmem_wait_ld();
+        } else {
+          // the whole accumulator is read and cleared: release it to the MMA
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
+        }
+        if (g & 1) {
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            // staging row `lane` is output row m_cta + 4 * lane + q
+            ptx::tma_store_3d(&tm_out, ptx::smem_u32(stg), n0 + 32 * (g - 1), m_cta / 4, q);
+            ptx::bulk_commit_group();
+          }
         }
       }
     }
@@ -842,13 +863,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t full_bar0 = to_leader(full(0));
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
       bool ok = true;
       for (int i = 0; i < n_items; ++i) {
         if (!warp_wait_bar<false>(auxfull(stage), phase, kSiteSfAuxFull, ctl)) {
           ok = false;
           break;
         }
-        if (i >= p.lora_blocks) {
+        if (i < p.lora_blocks) {
+          // LoRA item: this warp builds LA' rows [32q, 32q + 32)
+          uint8_t* st = smem + stage * L::kStageBytes;
+          if (p.lora_tma)
+            lora_la_from_smem(st + L::kLoraLA, st + L::kLoraRawLA, 32 * q, lane);
+          else
+            lora_la_direct<32>(st + L::kLoraLA, p, m_cta, i, 32 * q, lane);
+          ptx::fence_proxy_async_smem();
+        } else {
           const uint8_t* st = smem + stage * L::kStageBytes;
           // Every feeder writes the same words into its own lane quadrant:
           // the block-scaled MMA reads the scale words in every quadrant.
@@ -889,6 +921,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_before();
         }
         __syncwarp();
+        // The pair peer's LoRA rows are generic shared-memory writes that the
+        // leader's MMA reads: the proxy fence above orders them before this
+        // arrival (CTA-scope release, as for every other arrival here).
         if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
         if (++stage == S) {
           stage = 0;
