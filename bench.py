@@ -1,7 +1,7 @@
 """Throughput of the W4A4 NVFP4 + LoRA linear operator on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--dense]
 
 One step is one operator call (the whole path: scale relayout, LoRA operand
 prep, LoRA + block-scaled MMAs, fused affine epilogue) over one synthetic
@@ -13,7 +13,10 @@ launch on the launching stream, with L2 flushed (a 256 MiB memset, outside
 the events) before every timed launch.  `e2e` times the same call through
 the public API with the inputs copied from pinned host memory and the
 result copied back inside the timed region.  `--impl reference` times the
-CPU oracle on bounded row samples of the same workload.
+CPU oracle on bounded row samples of the same workload.  `--dense` runs the
+calibration variant of the workload: the same shape through the same kernel
+with R = 0 and no wcscale / bias, so the difference to the default run is
+the cost of the LoRA term and the affine epilogue.
 """
 
 from __future__ import annotations
@@ -43,6 +46,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="attn_proj_4096x3072x3072_r32")
+    ap.add_argument("--dense", action="store_true",
+                    help="calibration variant: R = 0, no wcscale, no bias")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -146,6 +151,16 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def workload_inputs(synth, w, dense: bool):
+    """The workload's seeded inputs; the dense calibration variant drops
+    wcscale and bias (the operator then uses 1 and 0) and has R = 0."""
+    inp = synth.make_workload_inputs(w)
+    if dense:
+        inp.pop("wcscale")
+        inp.pop("bias")
+    return inp
+
+
 def oracle_sample(w, inp, target_s=12.0, max_rows=None):
     """Time the oracle on a bounded row sample; returns (tflops, rows, seconds, threads)."""
     import numpy as np
@@ -173,7 +188,7 @@ def run_reference(args, w, rank):
         return
     from nvfp4_w4a4_quantized_gb300 import synth
 
-    inp = synth.make_workload_inputs(w)
+    inp = workload_inputs(synth, w, args.dense)
     per_step_target = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     _, rows, _, threads = oracle_sample(w, inp, target_s=per_step_target)
     import numpy as np
@@ -225,7 +240,7 @@ def run_ours(args, w, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
-    inp = synth.make_workload_inputs(w)
+    inp = workload_inputs(synth, w, args.dense)
     d = {k: v.to(dev) for k, v in inp.items()}
     out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
     opts = dict(tile_n=args.tile_n, stages=args.stages)
@@ -234,7 +249,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     def step(o=out, dd=d):
         pkg.svdq_w4a4_gemm(dd["act"], dd["wgt"], dd["ascales"], dd["wscales"], dd["lora_act_in"],
-                           dd["lora_up"], dd["wcscale"], dd["bias"], o, stream=stream,
+                           dd["lora_up"], dd.get("wcscale"), dd.get("bias"), o, stream=stream,
                            options=opts)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -350,6 +365,10 @@ def main():
     from nvfp4_w4a4_quantized_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
+    if args.dense:
+        import dataclasses
+
+        w = dataclasses.replace(w, name=w.name + "_dense", R=0)
     if args.impl == "reference":
         run_reference(args, w, rank)
     else:

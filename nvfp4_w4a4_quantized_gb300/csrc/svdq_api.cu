@@ -110,22 +110,50 @@ TileInfo tile_info_for(int cg, int bn) {
   return bn == 256 ? tile_info<1, 256>() : tile_info<1, 128>();
 }
 
-// Tile choice: a CTA pair (256 x 256 cluster tile) halves the operand bytes
-// each CTA streams per MMA; small problems that cannot fill the pairs fall
-// back to single-CTA tiles.
-void choose_tile(int64_t M, int64_t N, const svdq_options_t* o, int* cg, int* bn) {
-  int c = (o && o->cta_group) ? o->cta_group : 0;
-  int n = (o && o->tile_n) ? o->tile_n : 0;
-  if (c == 0) c = (n == 128 || M < 256 || N < 256) ? 1 : 2;
-  if (n == 0) n = (c == 2 || N >= 256) ? 256 : 128;
-  *cg = c;
-  *bn = n;
+// Tile choice.  Candidates: a CTA pair with a 256 x 256 cluster tile (each CTA
+// streams half the operand bytes per MMA), single CTAs with 128 x 256 or
+// 128 x 128 tiles.  Unless the caller forces one, the candidate with the least
+// estimated time wins: waves x per-SM tile work / relative efficiency, where
+// waves = ceil(tiles / (SMs / cg)) and the efficiencies (1, 0.87, 0.75) are the
+// measured large-shape throughputs relative to the pair.  A pair needs at
+// least 256 rows and columns (below that half its work would be padding).
+void choose_tile(int64_t M, int64_t N, const svdq_options_t* o, int sm_count, int* cg, int* bn) {
+  const int fc = (o && o->cta_group) ? o->cta_group : 0;
+  const int fn = (o && o->tile_n) ? o->tile_n : 0;
+  struct Cand {
+    int cg, bn;
+    double eff;
+  };
+  const Cand cands[3] = {{2, 256, 1.0}, {1, 256, 0.87}, {1, 128, 0.75}};
+  const int sms = sm_count > 0 ? sm_count : 1;
+  double best = 0.0;
+  int bc = 0, bb = 0;
+  for (const Cand& c : cands) {
+    if (fc && c.cg != fc) continue;
+    if (fn && c.bn != fn) continue;
+    if (c.cg == 2 && !fc && (M < 256 || N < 256)) continue;
+    const int64_t tiles = ((M + 128 * c.cg - 1) / (128 * c.cg)) * ((N + c.bn - 1) / c.bn);
+    const int64_t units = sms / c.cg > 0 ? sms / c.cg : 1;
+    const int64_t waves = (tiles + units - 1) / units;
+    const double cost = static_cast<double>(waves) * 128.0 * c.bn / c.eff;
+    if (bc == 0 || cost < best) {
+      best = cost;
+      bc = c.cg;
+      bb = c.bn;
+    }
+  }
+  if (bc == 0) {  // a forced combination outside the table (rejected later)
+    bc = fc ? fc : 1;
+    bb = fn ? fn : 256;
+  }
+  *cg = bc;
+  *bn = bb;
 }
 
 int make_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* o, int sm_count,
               int smem_optin, int max_clusters, Plan* out) {
   Plan pl;
-  choose_tile(M, N, o, &pl.cta_group, &pl.tile_n);
+  choose_tile(M, N, o, sm_count, &pl.cta_group, &pl.tile_n);
   const TileInfo ti = tile_info_for(pl.cta_group, pl.tile_n);
   // Pipeline depth: whatever shared memory is left after the epilogue staging,
   // per-warp wcscale/bias and barriers, capped by the tensor-memory columns
@@ -398,7 +426,7 @@ extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* a
   Plan pl;
   {
     int cg = 1, bn = 256;
-    choose_tile(M, N, options, &cg, &bn);
+    choose_tile(M, N, options, dinfo->sm_count, &cg, &bn);
     if (cg == 2)
       rc = ensure_kernel<2, 256>(dinfo, dinfo->smem_optin);
     else if (bn == 256)
