@@ -79,12 +79,16 @@ def scale_bytes(shape, g: torch.Generator) -> torch.Tensor:
     return (((u + 7) << 3) | i).to(torch.uint8)
 
 
-def make_inputs(M: int, N: int, K: int, R: int, seed: int) -> Dict[str, torch.Tensor]:
+def make_inputs(M: int, N: int, K: int, R: int, seed: int,
+                half: bool = False) -> Dict[str, torch.Tensor]:
     """Draw one set of operator inputs as contiguous CPU tensors.
 
     Returns a dict with keys act, wgt, ascales, wscales, lora_act_in,
-    lora_up, wcscale, bias (see the module docstring for layouts).
+    lora_up, wcscale, bias (see the module docstring for layouts).  With
+    ``half`` the same draws are rounded to fp16 instead of bf16 for lora_up,
+    wcscale and bias (the fp16 input/output variant).
     """
+    h16 = torch.float16 if half else torch.bfloat16
     if K % 16:
         raise ValueError("K must be a multiple of 16")
     g = torch.Generator(device="cpu")
@@ -94,9 +98,9 @@ def make_inputs(M: int, N: int, K: int, R: int, seed: int) -> Dict[str, torch.Te
     ascales = scale_bytes((K // 16, M), g)
     wscales = scale_bytes((K // 16, N), g)
     lora_act_in = torch.randn((M, R), generator=g, dtype=torch.float32)
-    lora_up = (torch.randn((N, R), generator=g, dtype=torch.float32) * 0.05).to(torch.bfloat16)
-    wcscale = (torch.rand((N,), generator=g, dtype=torch.float32) * 1.5 + 0.5).to(torch.bfloat16)
-    bias = (torch.randn((N,), generator=g, dtype=torch.float32) * 0.1).to(torch.bfloat16)
+    lora_up = (torch.randn((N, R), generator=g, dtype=torch.float32) * 0.05).to(h16)
+    wcscale = (torch.rand((N,), generator=g, dtype=torch.float32) * 1.5 + 0.5).to(h16)
+    bias = (torch.randn((N,), generator=g, dtype=torch.float32) * 0.1).to(h16)
     return dict(act=act.contiguous(), wgt=wgt.contiguous(), ascales=ascales.contiguous(),
                 wscales=wscales.contiguous(), lora_act_in=lora_act_in.contiguous(),
                 lora_up=lora_up.contiguous(), wcscale=wcscale.contiguous(), bias=bias.contiguous())

@@ -5,5 +5,5 @@ A plain CPU reference of the SVDQuant W4A4 linear operator in fp64
 check and bench.py's CPU-baseline leg may import it.
 """
 
-from .svdq_ref import (bf16_value, build, e2m1, e4m3, forward, num_threads,  # noqa: F401
-                       round_bf16_bits)
+from .svdq_ref import (bf16_value, build, e2m1, e4m3, f16_value, forward,  # noqa: F401
+                       num_threads, round_bf16_bits)

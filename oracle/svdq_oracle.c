@@ -22,7 +22,8 @@
  *   - wgt is [N, K/2] (K-major), i.e. the product is act . wgt^T;
  *   - the LoRA term is added after the wcscale multiply (it is not scaled);
  *   - lora_act_in is fp32 and used exactly; lora_up, wcscale and bias are
- *     bf16 and used exactly; a NULL wcscale means 1, a NULL bias means 0.
+ *     bf16 (or, in the fp16 variant the page also measures, IEEE binary16)
+ *     and used exactly; a NULL wcscale means 1, a NULL bias means 0.
  *
  * Parity pins (tests): the E2M1 table against the format's published value
  * set, E4M3 exhaustively against a library conversion, exact brute force in
@@ -73,6 +74,23 @@ double svdq_oracle_bf16(uint16_t bits) {
     return (double)f;
 }
 
+/* IEEE binary16 decoded bit by bit: sign = bit 15, exponent field e = bits
+ * 14..10 (bias 15), fraction f = bits 9..0.  e == 0 is subnormal
+ * 2^-14 * f/1024, e == 31 is infinity (f == 0) or NaN, otherwise the value is
+ * 2^(e-15) * (1 + f/1024). */
+double svdq_oracle_f16(uint16_t bits) {
+    int s = (bits >> 15) & 1;
+    int e = (bits >> 10) & 31;
+    int f = bits & 1023;
+    double v;
+    if (e == 31) return f ? NAN : (s ? -INFINITY : INFINITY);
+    if (e == 0)
+        v = ldexp((double)f / 1024.0, -14);
+    else
+        v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    return s ? -v : v;
+}
+
 /* Round an fp64 value to the nearest bf16 (ties to even), returning its bits.
  * Used only to report y in the output dtype; parity is judged on fp64 y. */
 uint16_t svdq_oracle_round_bf16(double x) {
@@ -114,23 +132,25 @@ static int nibble(const uint8_t* rowp, int64_t k) {
 
 /*
  * y[i][n] for every requested row m = rows[i] (all rows 0..M-1 when rows is
- * NULL) and every column n < N:
+ * NULL) and every column n < N (h16(x) below is bf16(x), or f16(x) when
+ * half_io is 1):
  *
  *   main(m,n) = sum_{g < K/16} e4m3(ascales[g][m]) * e4m3(wscales[g][n])
  *                             * sum_{k = 16g}^{16g+15} e2m1(a(m,k)) * e2m1(w(n,k))
- *   lora(m,n) = sum_{r < R} lora_act_in[m][r] * bf16(lora_up[n][r])
- *   y(m,n)    = bf16(wcscale[n]) * main(m,n) + bf16(bias[n]) + lora(m,n)
+ *   lora(m,n) = sum_{r < R} lora_act_in[m][r] * h16(lora_up[n][r])
+ *   y(m,n)    = h16(wcscale[n]) * main(m,n) + h16(bias[n]) + lora(m,n)
  *
  * main_out (nullable) receives main(m,n) in the same [nrows, N] layout.
  * Returns 0, or -1 for bad arguments / allocation failure.
  */
-int svdq_oracle_forward(const uint8_t* act, const uint8_t* wgt,
-                        const uint8_t* ascales, const uint8_t* wscales,
-                        const float* lora_act_in, const uint16_t* lora_up,
-                        const uint16_t* wcscale, const uint16_t* bias,
-                        int64_t M, int64_t N, int64_t K, int64_t R,
-                        const int64_t* rows, int64_t nrows,
-                        double* y, double* main_out) {
+int svdq_oracle_forward_io(const uint8_t* act, const uint8_t* wgt,
+                           const uint8_t* ascales, const uint8_t* wscales,
+                           const float* lora_act_in, const uint16_t* lora_up,
+                           const uint16_t* wcscale, const uint16_t* bias,
+                           int64_t M, int64_t N, int64_t K, int64_t R,
+                           const int64_t* rows, int64_t nrows,
+                           double* y, double* main_out, int half_io) {
+    double (*h16)(uint16_t) = half_io ? svdq_oracle_f16 : svdq_oracle_bf16;
     int64_t G, i, g, n;
     double* wsc;
     int bad = 0;
@@ -173,9 +193,9 @@ int svdq_oracle_forward(const uint8_t* act, const uint8_t* wgt,
                 mainv += asc[gg] * wsc[gg * N + nn] * s;
             }
             for (r = 0; r < R; ++r)
-                lora += (double)lora_act_in[m * R + r] * svdq_oracle_bf16(lora_up[nn * R + r]);
-            wc = wcscale ? svdq_oracle_bf16(wcscale[nn]) : 1.0;
-            b = bias ? svdq_oracle_bf16(bias[nn]) : 0.0;
+                lora += (double)lora_act_in[m * R + r] * h16(lora_up[nn * R + r]);
+            wc = wcscale ? h16(wcscale[nn]) : 1.0;
+            b = bias ? h16(bias[nn]) : 0.0;
             y[i * N + nn] = wc * mainv + b + lora;
             if (main_out) main_out[i * N + nn] = mainv;
         }
@@ -184,4 +204,16 @@ int svdq_oracle_forward(const uint8_t* act, const uint8_t* wgt,
     }
     free(wsc);
     return bad ? -1 : 0;
+}
+
+/* The bf16 operator (lora_up, wcscale, bias in bf16). */
+int svdq_oracle_forward(const uint8_t* act, const uint8_t* wgt,
+                        const uint8_t* ascales, const uint8_t* wscales,
+                        const float* lora_act_in, const uint16_t* lora_up,
+                        const uint16_t* wcscale, const uint16_t* bias,
+                        int64_t M, int64_t N, int64_t K, int64_t R,
+                        const int64_t* rows, int64_t nrows,
+                        double* y, double* main_out) {
+    return svdq_oracle_forward_io(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale,
+                                  bias, M, N, K, R, rows, nrows, y, main_out, 0);
 }

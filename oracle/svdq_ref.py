@@ -46,11 +46,16 @@ def _load():
             lib.svdq_oracle_e4m3.argtypes = [ctypes.c_int]
             lib.svdq_oracle_bf16.restype = d
             lib.svdq_oracle_bf16.argtypes = [ctypes.c_uint16]
+            lib.svdq_oracle_f16.restype = d
+            lib.svdq_oracle_f16.argtypes = [ctypes.c_uint16]
             lib.svdq_oracle_round_bf16.restype = ctypes.c_uint16
             lib.svdq_oracle_round_bf16.argtypes = [d]
             lib.svdq_oracle_num_threads.restype = ctypes.c_int
             lib.svdq_oracle_forward.restype = ctypes.c_int
             lib.svdq_oracle_forward.argtypes = [u8p] * 8 + [i64] * 4 + [u8p, i64, u8p, u8p]
+            lib.svdq_oracle_forward_io.restype = ctypes.c_int
+            lib.svdq_oracle_forward_io.argtypes = ([u8p] * 8 + [i64] * 4 +
+                                                   [u8p, i64, u8p, u8p, ctypes.c_int])
             _lib = lib
     return _lib
 
@@ -65,6 +70,10 @@ def e4m3(byte: int) -> float:
 
 def bf16_value(bits: int) -> float:
     return _load().svdq_oracle_bf16(int(bits) & 0xFFFF)
+
+
+def f16_value(bits: int) -> float:
+    return _load().svdq_oracle_f16(int(bits) & 0xFFFF)
 
 
 def round_bf16_bits(x: float) -> int:
@@ -85,7 +94,7 @@ def _np_bytes(t, dtype):
 
         if isinstance(t, torch.Tensor):
             t = t.detach().contiguous().cpu()
-            if t.dtype == torch.bfloat16:
+            if t.dtype in (torch.bfloat16, torch.float16):
                 t = t.view(torch.int16)
             t = t.numpy()
     except ImportError:  # pragma: no cover
@@ -94,14 +103,27 @@ def _np_bytes(t, dtype):
 
 
 def forward(inputs: Dict[str, object], M: int, N: int, K: int, R: int,
-            rows: Optional[Sequence[int]] = None, want_main: bool = False):
+            rows: Optional[Sequence[int]] = None, want_main: bool = False,
+            half_io: Optional[bool] = None):
     """Evaluate y (fp64) for the requested rows (all rows when None).
 
     ``inputs`` holds act, wgt, ascales, wscales, lora_act_in, lora_up,
     wcscale, bias (CPU torch tensors or numpy arrays; wcscale/bias may be
-    None).  Returns y [len(rows), N] float64, and main [len(rows), N] when
-    want_main is set.
+    None).  lora_up, wcscale and bias are bf16, or IEEE fp16 when
+    ``half_io`` (by default taken from the tensors' dtype).  Returns
+    y [len(rows), N] float64, and main [len(rows), N] when want_main is set.
     """
+    if half_io is None:
+        half_io = False
+        try:
+            import torch
+
+            for key in ("lora_up", "wcscale", "bias"):
+                t = inputs.get(key)
+                if isinstance(t, torch.Tensor) and t.dtype == torch.float16:
+                    half_io = True
+        except ImportError:  # pragma: no cover
+            pass
     lib = _load()
     act = _np_bytes(inputs["act"], np.uint8)
     wgt = _np_bytes(inputs["wgt"], np.uint8)
@@ -127,8 +149,9 @@ def forward(inputs: Dict[str, object], M: int, N: int, K: int, R: int,
     def p(a):
         return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
-    rc = lib.svdq_oracle_forward(p(act), p(wgt), p(asc), p(wsc), p(la), p(lu), p(wc), p(bi),
-                                 M, N, K, R, p(rows_arr), nrows, p(y), p(mo))
+    rc = lib.svdq_oracle_forward_io(p(act), p(wgt), p(asc), p(wsc), p(la), p(lu), p(wc), p(bi),
+                                    M, N, K, R, p(rows_arr), nrows, p(y), p(mo),
+                                    1 if half_io else 0)
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return (y, mo) if want_main else y

@@ -318,3 +318,62 @@ def test_nibble_order_invariance():
     # swapping only one operand does change it
     y3 = oracle.forward(dict(inp, act=swap(inp["act"])), M, N, K, R)
     assert not np.array_equal(y, y3)
+
+
+# --------------------------------------------------------------------------
+# the fp16 input/output variant (lora_up, wcscale, bias in IEEE binary16)
+
+def test_f16_decode_exhaustive_against_library():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    lib = torch.from_numpy(bits.view(np.int16)).view(torch.float16).to(torch.float64).numpy()
+    for b in range(0, 65536):
+        got = oracle.f16_value(b)
+        if math.isnan(lib[b]):
+            assert math.isnan(got), hex(b)
+        else:
+            assert got == lib[b] and math.copysign(1, got) == math.copysign(1, lib[b]), hex(b)
+
+
+@pytest.mark.parametrize("M,N,K,R,seed", [(3, 2, 32, 0, 41), (2, 5, 48, 1, 42), (5, 4, 64, 16, 43)])
+def test_exact_bruteforce_tiny_half(M, N, K, R, seed):
+    inp = synth.make_inputs(M, N, K, R, seed, half=True)
+    y = oracle.forward(inp, M, N, K, R)
+    # the rational brute force reads the fp16 values through the library
+    as_frac = lambda t: [Fraction(v) for v in t.to(torch.float64).flatten().tolist()]
+    a = nibbles(inp["act"].numpy())
+    w = nibbles(inp["wgt"].numpy())
+    sa = e4m3_library(inp["ascales"].numpy())
+    sw = e4m3_library(inp["wscales"].numpy())
+    wc, bi = as_frac(inp["wcscale"]), as_frac(inp["bias"])
+    lu = as_frac(inp["lora_up"])
+    la = inp["lora_act_in"].numpy().astype(np.float64)
+    for m in range(M):
+        for n in range(N):
+            main = Fraction(0)
+            for g in range(K // 16):
+                s = sum(e2m1_bits_fraction(int(a[m, k])) * e2m1_bits_fraction(int(w[n, k]))
+                        for k in range(16 * g, 16 * g + 16))
+                main += Fraction(float(sa[g, m])) * Fraction(float(sw[g, n])) * s
+            lora = sum(Fraction(float(la[m, r])) * lu[n * R + r] for r in range(R))
+            exact = wc[n] * main + bi[n] + lora
+            mag = abs(exact) + sum(abs(Fraction(float(la[m, r])) * lu[n * R + r]) for r in range(R))
+            assert abs(Fraction(y[m, n]) - exact) <= Fraction(2) ** -50 * (mag + 1), (m, n)
+
+
+def test_half_and_bf16_agree_on_shared_values():
+    # values exactly representable in both formats give the same y
+    M, N, K, R = 7, 9, 64, 16
+    inp = synth.make_inputs(M, N, K, R, 44)
+    g = torch.Generator().manual_seed(45)
+    shared = lambda shape: (torch.randint(-64, 64, shape, generator=g).to(torch.float32) / 64.0)
+    lu, wc, bi = shared((N, R)), shared((N,)) + 2.0, shared((N,))
+    y_b = oracle.forward(dict(inp, lora_up=lu.to(torch.bfloat16), wcscale=wc.to(torch.bfloat16),
+                              bias=bi.to(torch.bfloat16)), M, N, K, R)
+    y_h = oracle.forward(dict(inp, lora_up=lu.to(torch.float16), wcscale=wc.to(torch.float16),
+                              bias=bi.to(torch.float16)), M, N, K, R)
+    assert np.array_equal(y_b, y_h)
+    # and different fp16 values do change it (the dtype switch is live)
+    y_h2 = oracle.forward(dict(inp, lora_up=(lu * 1.0009765625).to(torch.float16),
+                               wcscale=wc.to(torch.float16), bias=bi.to(torch.float16)),
+                          M, N, K, R)
+    assert not np.array_equal(y_h, y_h2)
