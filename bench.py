@@ -1,7 +1,7 @@
 """Throughput of the W4A4 NVFP4 + LoRA linear operator on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--dense]
+                    [--workload NAME] [--dense] [--fp16]
 
 One step is one operator call (the whole path: scale relayout, LoRA operand
 prep, LoRA + block-scaled MMAs, fused affine epilogue) over one synthetic
@@ -16,7 +16,8 @@ result copied back inside the timed region.  `--impl reference` times the
 CPU oracle on bounded row samples of the same workload.  `--dense` runs the
 calibration variant of the workload: the same shape through the same kernel
 with R = 0 and no wcscale / bias, so the difference to the default run is
-the cost of the LoRA term and the affine epilogue.
+the cost of the LoRA term and the affine epilogue.  `--fp16` runs the fp16
+input/output variant (lora_up, wcscale, bias and y in IEEE fp16).
 """
 
 from __future__ import annotations
@@ -48,6 +49,8 @@ def parse():
     ap.add_argument("--workload", default="attn_proj_4096x3072x3072_r32")
     ap.add_argument("--dense", action="store_true",
                     help="calibration variant: R = 0, no wcscale, no bias")
+    ap.add_argument("--fp16", action="store_true",
+                    help="fp16 input/output variant (lora_up, wcscale, bias, y in fp16)")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -151,10 +154,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def workload_inputs(synth, w, dense: bool):
+def workload_inputs(synth, w, dense: bool, half: bool = False):
     """The workload's seeded inputs; the dense calibration variant drops
-    wcscale and bias (the operator then uses 1 and 0) and has R = 0."""
-    inp = synth.make_workload_inputs(w)
+    wcscale and bias (the operator then uses 1 and 0) and has R = 0; the fp16
+    variant draws the same values rounded to fp16."""
+    inp = synth.make_inputs(w.M, w.N, w.K, w.R, w.seed, half=half)
     if dense:
         inp.pop("wcscale")
         inp.pop("bias")
@@ -188,7 +192,7 @@ def run_reference(args, w, rank):
         return
     from nvfp4_w4a4_quantized_gb300 import synth
 
-    inp = workload_inputs(synth, w, args.dense)
+    inp = workload_inputs(synth, w, args.dense, args.fp16)
     per_step_target = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     _, rows, _, threads = oracle_sample(w, inp, target_s=per_step_target)
     import numpy as np
@@ -240,9 +244,10 @@ def run_ours(args, w, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
-    inp = workload_inputs(synth, w, args.dense)
+    inp = workload_inputs(synth, w, args.dense, args.fp16)
     d = {k: v.to(dev) for k, v in inp.items()}
-    out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+    out_dtype = torch.float16 if args.fp16 else torch.bfloat16
+    out = torch.empty((w.M, w.N), dtype=out_dtype, device=dev)
     opts = dict(tile_n=args.tile_n, stages=args.stages)
     plan = pkg.svdq_query_plan(w.M, w.N, w.K, w.R, options=opts)
     stream = torch.cuda.current_stream(dev)
@@ -287,7 +292,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     # end to end through the public call: pinned host inputs -> device -> op -> host
     host = {k: v.pin_memory() for k, v in inp.items()}
-    host_out = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    host_out = torch.empty((w.M, w.N), dtype=out_dtype).pin_memory()
     dd = {k: torch.empty_like(v, device=dev) for k, v in inp.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = host_out.numel() * host_out.element_size()
@@ -365,10 +370,13 @@ def main():
     from nvfp4_w4a4_quantized_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
-    if args.dense:
+    if args.dense or args.fp16:
         import dataclasses
 
-        w = dataclasses.replace(w, name=w.name + "_dense", R=0)
+        if args.dense:
+            w = dataclasses.replace(w, name=w.name + "_dense", R=0)
+        if args.fp16:
+            w = dataclasses.replace(w, name=w.name + "_fp16")
     if args.impl == "reference":
         run_reference(args, w, rank)
     else:

@@ -42,6 +42,10 @@ extern "C" {
 #define SVDQ_MAX_K (1LL << 20)
 #define SVDQ_MAX_RANK 128
 
+/* 16-bit I/O types (svdq_options_t.io_dtype). */
+#define SVDQ_IO_BF16 0
+#define SVDQ_IO_FP16 1
+
 /*
  * svdq_w4a4_gemm -- y = scaled_mma(act4, wgt4) * wcscale + bias + lora_act_in @ lora_up
  * ("SVDQuant W4A4 on Blackwell" §2, §3.1, and the fused epilogue of §6.6).
@@ -90,15 +94,22 @@ typedef struct svdq_options {
     int32_t stages;      /* 0 = pipeline-depth solver's choice; else forced (2..8)  */
     int32_t max_ctas;    /* 0 = one persistent CTA per SM; else cap on the grid    */
     int32_t timeout_ms;  /* bounded-wait limit inside the kernel; 0 = 2000 ms       */
-    int32_t debug_fault; /* tests only: 1 starts the accumulator producer at the
-                            wrong phase, so the kernel must time out and report
-                            SVDQ_ERR_TIMEOUT instead of hanging                    */
+    int32_t debug_fault; /* tests only: 1 makes the MMA issuers wait on a barrier
+                            no role arrives on, so the kernel must time out and
+                            report SVDQ_ERR_TIMEOUT instead of hanging             */
     int32_t cta_group;   /* 0 = planner's choice; 1 = one CTA per MMA, 2 = a CTA pair
                             issuing 256-row MMAs (tile_n must then be 256)           */
-    int32_t reserved[2]; /* must be zero                                            */
+    int32_t io_dtype;    /* 16-bit I/O type of lora_up, wcscale, bias and out:
+                            SVDQ_IO_BF16 (0, default) or SVDQ_IO_FP16 (1, IEEE
+                            binary16; LoRA operands are then rounded to fp16) */
+    int32_t reserved;    /* must be zero                                            */
 } svdq_options_t;
 
-/* svdq_w4a4_gemm with options; identical semantics otherwise. */
+/* svdq_w4a4_gemm with options; identical semantics otherwise.  With
+ * io_dtype = SVDQ_IO_FP16, lora_up, wcscale, bias and out hold IEEE fp16 in
+ * the same shapes (the fp16 variant "SVDQuant W4A4 on Blackwell" §8 also
+ * measures): y is rounded to fp16 (RNE) and the LoRA operands LA' = f16(LA),
+ * LU' = f16(LU / wcscale) are fp16 on the tensor cores. */
 int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* ascales, const void* wscales,
                       const float* lora_act_in, const void* lora_up, const void* wcscale,
                       const void* bias, void* out, int64_t M, int64_t N, int64_t K, int64_t R,

@@ -25,6 +25,9 @@ SVDQ_ERR_CUDA = -6
 SVDQ_ERR_TIMEOUT = -7
 SVDQ_ERR_BAD_OPTION = -8
 
+SVDQ_IO_BF16 = 0
+SVDQ_IO_FP16 = 1
+
 # Every symbol include/svdq.h declares.
 EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_query_plan", "svdq_lora_stage_bytes",
             "svdq_read_device_status", "svdq_status_string", "svdq_version")
@@ -34,7 +37,7 @@ class SvdqOptions(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("debug_fault", ctypes.c_int32), ("cta_group", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("io_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class SvdqPlan(ctypes.Structure):
@@ -139,7 +142,9 @@ def svdq_w4a4_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bi
     Tensors are CUDA torch tensors with the layouts of include/svdq.h
     (act uint8 [M, K/2], wgt uint8 [N, K/2], ascales uint8 [K/16, M],
     wscales uint8 [K/16, N], lora_act_in fp32 [M, R], lora_up bf16 [N, R],
-    wcscale/bias bf16 [N] or None, out bf16 [M, N]).  Asynchronous on
+    wcscale/bias bf16 [N] or None, out bf16 [M, N]).  An fp16 ``out`` selects
+    the fp16 variant: lora_up, wcscale and bias must then be fp16 too.
+    Asynchronous on
     ``stream`` (default: torch's current stream).  Raises SvdqError on a
     non-zero status when ``check``; returns the status otherwise.
     """
@@ -149,11 +154,12 @@ def svdq_w4a4_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bi
     N = wgt.shape[0]
     K = 2 * kh
     R = 0 if lora_act_in is None else int(lora_act_in.shape[1])
+    h16 = torch.float16 if out.dtype == torch.float16 else torch.bfloat16
     for name, t, dt in (("act", act, torch.uint8), ("wgt", wgt, torch.uint8),
                         ("ascales", ascales, torch.uint8), ("wscales", wscales, torch.uint8),
                         ("lora_act_in", lora_act_in, torch.float32),
-                        ("lora_up", lora_up, torch.bfloat16), ("wcscale", wcscale, torch.bfloat16),
-                        ("bias", bias, torch.bfloat16), ("out", out, torch.bfloat16)):
+                        ("lora_up", lora_up if R else None, h16), ("wcscale", wcscale, h16),
+                        ("bias", bias, h16), ("out", out, h16)):
         if t is None:
             continue
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
@@ -170,6 +176,9 @@ def svdq_w4a4_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bi
     lib = load()
     h = _stream_handle(stream, act.device)
     opts = _opts(options)
+    if h16 == torch.float16:
+        opts = opts if opts is not None else SvdqOptions()
+        opts.io_dtype = SVDQ_IO_FP16
     args = [_ptr(act), _ptr(wgt), _ptr(ascales), _ptr(wscales), _ptr(lora_act_in),
             _ptr(lora_up), _ptr(wcscale), _ptr(bias), _ptr(out), M, N, K, R]
     with torch.cuda.device(act.device):

@@ -31,8 +31,9 @@ struct DeviceInfo {
   int sm_count = 0;
   int smem_optin = 0;
   int* status = nullptr;
-  bool attr_set[3] = {false, false, false};  // (1,128), (1,256), (2,256)
-  int max_clusters[3] = {0, 0, 0};
+  // per kernel: (1,128), (1,256), (2,256) with bf16 I/O, then the same with fp16
+  bool attr_set[6] = {false, false, false, false, false, false};
+  int max_clusters[6] = {0, 0, 0, 0, 0, 0};
 };
 
 std::mutex g_mutex;
@@ -68,8 +69,8 @@ int validate_options(const svdq_options_t* o) {
   if (o->debug_fault != 0 && o->debug_fault != 1) return SVDQ_ERR_BAD_OPTION;
   if (o->cta_group < 0 || o->cta_group > 2) return SVDQ_ERR_BAD_OPTION;
   if (o->cta_group == 2 && o->tile_n == 128) return SVDQ_ERR_BAD_OPTION;
-  for (int r : o->reserved)
-    if (r != 0) return SVDQ_ERR_BAD_OPTION;
+  if (o->io_dtype != SVDQ_IO_BF16 && o->io_dtype != SVDQ_IO_FP16) return SVDQ_ERR_BAD_OPTION;
+  if (o->reserved != 0) return SVDQ_ERR_BAD_OPTION;
   return SVDQ_OK;
 }
 
@@ -244,19 +245,18 @@ int probe_device(int* dev_out, DeviceInfo** info_out) {
   return SVDQ_OK;
 }
 
-template <int CG, int BN>
-constexpr int kernel_index() {
-  return CG == 2 ? 2 : (BN == 256 ? 1 : 0);
+constexpr int kernel_index(int cg, int bn, bool f16) {
+  return (cg == 2 ? 2 : (bn == 256 ? 1 : 0)) + (f16 ? 3 : 0);
 }
 
 // Once per device and kernel: opt in to the shared memory and find how many
 // clusters fit at once.
-template <int CG, int BN>
+template <int CG, int BN, bool F16>
 int ensure_kernel(DeviceInfo* d, int smem_bytes) {
   std::lock_guard<std::mutex> lock(g_mutex);
-  const int idx = kernel_index<CG, BN>();
+  const int idx = kernel_index(CG, BN, F16);
   if (!d->attr_set[idx]) {
-    auto k = svdq_w4a4_kernel<CG, BN, kbi_for<CG>()>;
+    auto k = svdq_w4a4_kernel<CG, BN, kbi_for<CG>(), F16>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -310,11 +310,13 @@ struct Operands {
   void* out;
 };
 
-template <int CG, int BN>
+template <int CG, int BN, bool F16>
 int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams& kp, int64_t M,
            int64_t N, int64_t K, int64_t R, cudaStream_t stream) {
   constexpr int KBI = kbi_for<CG>();
   using L = Layout<CG, BN, KBI>;
+  constexpr CUtensorMapDataType kIoType =
+      F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   (void)dinfo;
   int rc = SVDQ_OK;
   alignas(64) CUtensorMap tm[8];
@@ -349,7 +351,7 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
     const uint64_t d_out[3] = {static_cast<uint64_t>(N), M4, 4},
                    s_out[2] = {static_cast<uint64_t>(N) * 8, static_cast<uint64_t>(N) * 2};
     const uint32_t b_out[3] = {64, 32, 1};
-    if ((rc = encode(&tm[7], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, op.out, d_out, s_out, b_out,
+    if ((rc = encode(&tm[7], kIoType, 3, op.out, d_out, s_out, b_out,
                      CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
       return rc;
   }
@@ -361,7 +363,7 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
                      CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
       return rc;
     const uint64_t d_lu[3] = {r64, N4, 4}, s_lu[2] = {8 * r64, 2 * r64};
-    if ((rc = encode(&tm[5], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, op.lu, d_lu, s_lu, b_lora,
+    if ((rc = encode(&tm[5], kIoType, 3, op.lu, d_lu, s_lu, b_lora,
                      CU_TENSOR_MAP_SWIZZLE_64B)) != SVDQ_OK)
       return rc;
   } else {
@@ -371,7 +373,7 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
   if (op.wc != nullptr) {
     const uint64_t d_wc[1] = {static_cast<uint64_t>(N)};
     const uint32_t b_wc[1] = {L::kBNc};
-    if ((rc = encode(&tm[6], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 1, op.wc, d_wc, nullptr, b_wc,
+    if ((rc = encode(&tm[6], kIoType, 1, op.wc, d_wc, nullptr, b_wc,
                      CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
       return rc;
   } else {
@@ -389,7 +391,7 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CG == 2 ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, svdq_w4a4_kernel<CG, BN, KBI>, tm[0], tm[1], tm[2],
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, svdq_w4a4_kernel<CG, BN, KBI, F16>, tm[0], tm[1], tm[2],
                                            tm[3], tm[4], tm[5], tm[6], tm[7], kp);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -412,6 +414,7 @@ extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* a
                                  const svdq_options_t* options, void* stream) {
   int rc = validate_options(options);
   if (rc != SVDQ_OK) return rc;
+  const bool f16 = options != nullptr && options->io_dtype == SVDQ_IO_FP16;
   if (!act || !wgt || !ascales || !wscales || !out) return SVDQ_ERR_INVALID_ARG;
   if (R > 0 && (!lora_act_in || !lora_up)) return SVDQ_ERR_INVALID_ARG;
   if ((rc = validate_shape(M, N, K, R)) != SVDQ_OK) return rc;
@@ -428,13 +431,16 @@ extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* a
     int cg = 1, bn = 256;
     choose_tile(M, N, options, dinfo->sm_count, &cg, &bn);
     if (cg == 2)
-      rc = ensure_kernel<2, 256>(dinfo, dinfo->smem_optin);
+      rc = f16 ? ensure_kernel<2, 256, true>(dinfo, dinfo->smem_optin)
+               : ensure_kernel<2, 256, false>(dinfo, dinfo->smem_optin);
     else if (bn == 256)
-      rc = ensure_kernel<1, 256>(dinfo, dinfo->smem_optin);
+      rc = f16 ? ensure_kernel<1, 256, true>(dinfo, dinfo->smem_optin)
+               : ensure_kernel<1, 256, false>(dinfo, dinfo->smem_optin);
     else
-      rc = ensure_kernel<1, 128>(dinfo, dinfo->smem_optin);
+      rc = f16 ? ensure_kernel<1, 128, true>(dinfo, dinfo->smem_optin)
+               : ensure_kernel<1, 128, false>(dinfo, dinfo->smem_optin);
     if (rc != SVDQ_OK) return rc;
-    const int idx = cg == 2 ? 2 : (bn == 256 ? 1 : 0);
+    const int idx = kernel_index(cg, bn, f16);
     if ((rc = make_plan(M, N, K, R, options, dinfo->sm_count, dinfo->smem_optin,
                         dinfo->max_clusters[idx], &pl)) != SVDQ_OK)
       return rc;
@@ -460,16 +466,21 @@ extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* a
   const int tmo = (options && options->timeout_ms) ? options->timeout_ms : kDefaultTimeoutMs;
   kp.timeout_ns = static_cast<unsigned long long>(tmo) * 1000000ull;
   kp.lora_act_in = R > 0 ? lora_act_in : nullptr;
-  kp.lora_up = R > 0 ? static_cast<const __nv_bfloat16*>(lora_up) : nullptr;
-  kp.wcscale = static_cast<const __nv_bfloat16*>(wcscale);
-  kp.bias = static_cast<const __nv_bfloat16*>(bias);
+  kp.lora_up = R > 0 ? static_cast<const uint16_t*>(lora_up) : nullptr;
+  kp.wcscale = static_cast<const uint16_t*>(wcscale);
+  kp.bias = static_cast<const uint16_t*>(bias);
   kp.status = dinfo->status;
 
   const Operands op{act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (pl.cta_group == 2) return launch<2, 256>(pl, dinfo, op, kp, M, N, K, R, s);
-  if (pl.tile_n == 256) return launch<1, 256>(pl, dinfo, op, kp, M, N, K, R, s);
-  return launch<1, 128>(pl, dinfo, op, kp, M, N, K, R, s);
+  if (f16) {
+    if (pl.cta_group == 2) return launch<2, 256, true>(pl, dinfo, op, kp, M, N, K, R, s);
+    if (pl.tile_n == 256) return launch<1, 256, true>(pl, dinfo, op, kp, M, N, K, R, s);
+    return launch<1, 128, true>(pl, dinfo, op, kp, M, N, K, R, s);
+  }
+  if (pl.cta_group == 2) return launch<2, 256, false>(pl, dinfo, op, kp, M, N, K, R, s);
+  if (pl.tile_n == 256) return launch<1, 256, false>(pl, dinfo, op, kp, M, N, K, R, s);
+  return launch<1, 128, false>(pl, dinfo, op, kp, M, N, K, R, s);
 }
 
 extern "C" int svdq_w4a4_gemm(const void* act, const void* wgt, const void* ascales,

@@ -65,6 +65,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -162,9 +163,9 @@ struct KParams {
   int debug_fault;
   unsigned long long timeout_ns;
   const float* lora_act_in;
-  const __nv_bfloat16* lora_up;
-  const __nv_bfloat16* wcscale;
-  const __nv_bfloat16* bias;
+  const uint16_t* lora_up;  // bf16 or fp16 bits (the kernel's 16-bit I/O type)
+  const uint16_t* wcscale;
+  const uint16_t* bias;
   int* status;
 };
 
@@ -245,6 +246,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// The 16-bit I/O type of lora_up, wcscale, bias and the output: bf16 (the
+// operator as stated) or IEEE fp16 (the variant the page also measures).
+// lo/hi decode the halves of a packed pair, pack rounds two fp32 values (RNE).
+template <bool F16>
+struct H16 {
+  static __device__ __forceinline__ float one(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+  static __device__ __forceinline__ float lo(uint32_t w) { return bf16_lo(w); }
+  static __device__ __forceinline__ float hi(uint32_t w) { return bf16_hi(w); }
+  static __device__ __forceinline__ uint32_t pack(float a, float b) { return ptx::pack_bf16x2(a, b); }
+  static constexpr uint32_t kOnes = 0x3F803F80u;  // (1.0, 1.0)
+};
+template <>
+struct H16<true> {
+  static __device__ __forceinline__ float one(uint16_t b) {
+    return __half2float(__ushort_as_half(b));
+  }
+  static __device__ __forceinline__ float lo(uint32_t w) { return one(uint16_t(w & 0xFFFFu)); }
+  static __device__ __forceinline__ float hi(uint32_t w) { return one(uint16_t(w >> 16)); }
+  static __device__ __forceinline__ uint32_t pack(float a, float b) { return ptx::pack_f16x2(a, b); }
+  static constexpr uint32_t kOnes = 0x3C003C00u;
+};
+
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
@@ -285,6 +308,7 @@ __device__ __forceinline__ int sw64_offset(int row, int chunk) {
 // LA' rows r0 .. r0+31 from the TMA-staged raw fp32 rows [128][32] (already in
 // row-quad order): lane reads 4 consecutive floats of a row, writes 4 bf16
 // (half a 16-byte chunk).
+template <bool F16>
 __device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* raw, int r0,
                                                   int lane) {
   const int c = lane & 7;  // 16-byte piece of the 128-byte raw row
@@ -293,22 +317,21 @@ __device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* r
     const int row = r0 + it * 4 + (lane >> 3);
     const float4 v = *reinterpret_cast<const float4*>(raw + row * 128 + 16 * c);
     uint2 pk;
-    pk.x = ptx::pack_bf16x2(v.x, v.y);
-    pk.y = ptx::pack_bf16x2(v.z, v.w);
+    pk.x = H16<F16>::pack(v.x, v.y);
+    pk.y = H16<F16>::pack(v.z, v.w);
     *reinterpret_cast<uint2*>(dst + sw64_offset(row, c >> 1) + 8 * (c & 1)) = pk;
   }
 }
 
 // 1/wcscale for tile rows r0 + lane + 32t (t < NR/32), 0 outside N or for a
 // zero wcscale (fp32 reciprocal, correctly rounded).
-template <int NR>
+template <int NR, bool F16>
 __device__ __forceinline__ void lora_inv_wc(float* inv, const uint8_t* wc, int n_cta, int N,
                                             int r0, int lane) {
 #pragma unroll
   for (int t = 0; t < NR / 32; ++t) {
     const int off = quad_row(r0 + lane + 32 * t);
-    const float w = __uint_as_float(static_cast<uint32_t>(
-                        *reinterpret_cast<const uint16_t*>(wc + 2 * off)) << 16);
+    const float w = H16<F16>::one(*reinterpret_cast<const uint16_t*>(wc + 2 * off));
     inv[t] = (n_cta + off < N && w != 0.f) ? __frcp_rn(w) : 0.f;
   }
 }
@@ -318,21 +341,22 @@ __device__ __forceinline__ void lora_inv_wc(float* inv, const uint8_t* wc, int n
 // staged wcscale is in plain column order.  Rows outside N (zero-filled) stay
 // zero.  Each row's reciprocal is computed once and shuffled to the row's
 // four lanes.
-template <int NR>
+template <int NR, bool F16>
 __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* wc, int n_cta,
                                                    int N, int r0, int lane) {
+  using H = H16<F16>;
   float inv[NR / 32];
-  lora_inv_wc<NR>(inv, wc, n_cta, N, r0, lane);
+  lora_inv_wc<NR, F16>(inv, wc, n_cta, N, r0, lane);
   const int pc = lane & 3;
 #pragma unroll
   for (int it = 0; it < NR / 8; ++it) {
     const int row = r0 + it * 8 + (lane >> 2);
     const float s = __shfl_sync(0xffffffffu, inv[it / 4], (it % 4) * 8 + (lane >> 2));
     uint4 x = *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc);
-    x.x = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.x), s), __fmul_rn(bf16_hi(x.x), s));
-    x.y = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.y), s), __fmul_rn(bf16_hi(x.y), s));
-    x.z = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.z), s), __fmul_rn(bf16_hi(x.z), s));
-    x.w = ptx::pack_bf16x2(__fmul_rn(bf16_lo(x.w), s), __fmul_rn(bf16_hi(x.w), s));
+    x.x = H::pack(__fmul_rn(H::lo(x.x), s), __fmul_rn(H::hi(x.x), s));
+    x.y = H::pack(__fmul_rn(H::lo(x.y), s), __fmul_rn(H::hi(x.y), s));
+    x.z = H::pack(__fmul_rn(H::lo(x.z), s), __fmul_rn(H::hi(x.z), s));
+    x.w = H::pack(__fmul_rn(H::lo(x.w), s), __fmul_rn(H::hi(x.w), s));
     *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc) = x;
   }
 }
@@ -341,7 +365,7 @@ __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* w
 // are not 16-byte strided for TMA): LA' tile row r holds matrix row m_cta +
 // quad_row(r), LU' tile row r column n_cta + quad_row(r); ranks 32*blk ..
 // 32*blk+31, zero outside [M|N, R).  Rows r0 .. r0+NR-1.
-template <int NR>
+template <int NR, bool F16>
 __device__ __forceinline__ void lora_la_direct(uint8_t* dst, const KParams& p, int m_cta, int blk,
                                                int r0, int lane) {
   const int chunk = lane & 3;
@@ -354,47 +378,45 @@ __device__ __forceinline__ void lora_la_direct(uint8_t* dst, const KParams& p, i
     for (int q = 0; q < 8; ++q)
       v[q] = (m < p.M && k0 + q < p.R) ? __ldg(p.lora_act_in + (size_t)m * p.R + k0 + q) : 0.f;
     uint4 pk;
-    pk.x = ptx::pack_bf16x2(v[0], v[1]);
-    pk.y = ptx::pack_bf16x2(v[2], v[3]);
-    pk.z = ptx::pack_bf16x2(v[4], v[5]);
-    pk.w = ptx::pack_bf16x2(v[6], v[7]);
+    pk.x = H16<F16>::pack(v[0], v[1]);
+    pk.y = H16<F16>::pack(v[2], v[3]);
+    pk.z = H16<F16>::pack(v[4], v[5]);
+    pk.w = H16<F16>::pack(v[6], v[7]);
     *reinterpret_cast<uint4*>(dst + sw64_offset(row, chunk)) = pk;
   }
 }
 
-template <int NR>
+template <int NR, bool F16>
 __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p, int n_cta, int blk,
                                                int r0, int lane) {
   const int chunk = lane & 3;
   const int k0 = blk * kLoraRanks + chunk * 8;
-  const uint16_t* lu = reinterpret_cast<const uint16_t*>(p.lora_up);
-  const uint16_t* wc = reinterpret_cast<const uint16_t*>(p.wcscale);
+  const uint16_t* lu = p.lora_up;
+  const uint16_t* wc = p.wcscale;
   for (int it = 0; it < NR / 8; ++it) {
     const int row = r0 + it * 8 + (lane >> 2);
     const int n = n_cta + quad_row(row);
     float inv = 0.f;
     if (n < p.N) {
-      const float w = wc ? __uint_as_float(static_cast<uint32_t>(__ldg(wc + n)) << 16) : 1.f;
+      const float w = wc ? H16<F16>::one(__ldg(wc + n)) : 1.f;
       inv = (w != 0.f) ? __frcp_rn(w) : 0.f;
     }
     float v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
       v[q] = (n < p.N && k0 + q < p.R)
-                 ? __fmul_rn(__uint_as_float(static_cast<uint32_t>(
-                                 __ldg(lu + (size_t)n * p.R + k0 + q)) << 16),
-                             inv)
+                 ? __fmul_rn(H16<F16>::one(__ldg(lu + (size_t)n * p.R + k0 + q)), inv)
                  : 0.f;
     uint4 pk;
-    pk.x = ptx::pack_bf16x2(v[0], v[1]);
-    pk.y = ptx::pack_bf16x2(v[2], v[3]);
-    pk.z = ptx::pack_bf16x2(v[4], v[5]);
-    pk.w = ptx::pack_bf16x2(v[6], v[7]);
+    pk.x = H16<F16>::pack(v[0], v[1]);
+    pk.y = H16<F16>::pack(v[2], v[3]);
+    pk.z = H16<F16>::pack(v[4], v[5]);
+    pk.w = H16<F16>::pack(v[6], v[7]);
     *reinterpret_cast<uint4*>(dst + sw64_offset(row, chunk)) = pk;
   }
 }
 
-template <int CG, int BN, int KBI>
+template <int CG, int BN, int KBI, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     svdq_w4a4_kernel(const __grid_constant__ CUtensorMap tm_act,
                      const __grid_constant__ CUtensorMap tm_wgt,
@@ -594,7 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int tile_iter = 0;
       constexpr uint32_t kIdescMain = ptx::idesc_mxf4nvf4(kBM * CG, BN);
-      constexpr uint32_t kIdescLora = ptx::idesc_bf16_f32(kBM * CG, BN);
+      constexpr uint32_t kIdescLora =
+          F16 ? ptx::idesc_f16_f32(kBM * CG, BN) : ptx::idesc_bf16_f32(kBM * CG, BN);
       const uint64_t desc_a0 = ptx::desc_kmajor_sw128(sbase + L::kOffA);
       const uint64_t desc_b0 = ptx::desc_kmajor_sw128(sbase + L::kOffB);
       const bool k_ragged = (p.K % kBK) != 0;  // the last K block is partial
@@ -716,10 +739,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + stage * L::kStageBytes;
           const int r0 = (warp - 2) * (L::kBNc / 2);
           if (!p.lora_tma)
-            lora_lu_direct<L::kBNc / 2>(st + L::kLoraLU, p, n_cta, i, r0, lane);
+            lora_lu_direct<L::kBNc / 2, F16>(st + L::kLoraLU, p, n_cta, i, r0, lane);
           else if (p.wcscale != nullptr)
-            lora_lu_scale_smem<L::kBNc / 2>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, r0,
-                                            lane);
+            lora_lu_scale_smem<L::kBNc / 2, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N,
+                                                 r0, lane);
           ptx::fence_proxy_async_smem();
         }
         __syncwarp();
@@ -737,8 +760,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quadrant of this warp
-    const uint16_t* wcg = reinterpret_cast<const uint16_t*>(p.wcscale);
-    const uint16_t* big = reinterpret_cast<const uint16_t*>(p.bias);
+    using H = H16<F16>;
+    const uint16_t* wcg = p.wcscale;
+    const uint16_t* big = p.bias;
     uint8_t* stg = smem + L::epi_offset(S) + q * L::kEpiStageBytes;
     float* wb = reinterpret_cast<float*>(smem + L::wcb_offset(S) + q * (8 * BN));  // wc, bias
     const uint32_t acc_empty0 = to_leader(acc_empty(0));
@@ -764,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warp reads it; the previous tile's reads are behind us in program order).
       if (lane < BN / 8) {
         const int c = 8 * lane;
-        uint4 wv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // 1.0
+        uint4 wv = make_uint4(H::kOnes, H::kOnes, H::kOnes, H::kOnes);  // 1.0
         uint4 bv = make_uint4(0u, 0u, 0u, 0u);
         if (n0 + c < p.N) {
           if (wcg) wv = __ldg(reinterpret_cast<const uint4*>(wcg + n0 + c));
@@ -774,11 +798,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           *reinterpret_cast<float4*>(wb + c + 4 * i) =
-              make_float4(bf16_lo(w4[2 * i]), bf16_hi(w4[2 * i]), bf16_lo(w4[2 * i + 1]),
-                          bf16_hi(w4[2 * i + 1]));
+              make_float4(H::lo(w4[2 * i]), H::hi(w4[2 * i]), H::lo(w4[2 * i + 1]),
+                          H::hi(w4[2 * i + 1]));
           *reinterpret_cast<float4*>(wb + BN + c + 4 * i) =
-              make_float4(bf16_lo(b4[2 * i]), bf16_hi(b4[2 * i]), bf16_lo(b4[2 * i + 1]),
-                          bf16_hi(b4[2 * i + 1]));
+              make_float4(H::lo(b4[2 * i]), H::hi(b4[2 * i]), H::lo(b4[2 * i + 1]),
+                          H::hi(b4[2 * i + 1]));
         }
       }
       __syncwarp();
@@ -825,8 +849,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float y1 = fmaf(__uint_as_float(cur[1][k]), w.y, bb.y);
           const float y2 = fmaf(__uint_as_float(cur[2][k]), w.z, bb.z);
           const float y3 = fmaf(__uint_as_float(cur[3][k]), w.w, bb.w);
-          pk[2 * k] = ptx::pack_bf16x2(y0, y1);
-          pk[2 * k + 1] = ptx::pack_bf16x2(y2, y3);
+          pk[2 * k] = H::pack(y0, y1);
+          pk[2 * k + 1] = H::pack(y2, y3);
         }
         // 16-byte chunk j of the 128-byte staging row holds columns 8j .. 8j+7
 #pragma unroll
@@ -876,9 +900,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // LoRA item: this warp builds LA' rows [32q, 32q + 32)
           uint8_t* st = smem + stage * L::kStageBytes;
           if (p.lora_tma)
-            lora_la_from_smem(st + L::kLoraLA, st + L::kLoraRawLA, 32 * q, lane);
+            lora_la_from_smem<F16>(st + L::kLoraLA, st + L::kLoraRawLA, 32 * q, lane);
           else
-            lora_la_direct<32>(st + L::kLoraLA, p, m_cta, i, 32 * q, lane);
+            lora_la_direct<32, F16>(st + L::kLoraLA, p, m_cta, i, 32 * q, lane);
           ptx::fence_proxy_async_smem();
         } else {
           const uint8_t* st = smem + stage * L::kStageBytes;

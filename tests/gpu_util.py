@@ -20,7 +20,12 @@ def run_gpu(inp, M, N, K, R, options=None, check_status=True):
     `out` is pre-filled with NaN so an element the kernel fails to write is
     caught by the finiteness check."""
     d = to_device(inp)
-    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    # the 16-bit I/O type follows the inputs (fp16 lora_up / wcscale / bias
+    # select the fp16 variant)
+    half = any(isinstance(inp.get(k), torch.Tensor) and inp[k].dtype == torch.float16
+               for k in ("lora_up", "wcscale", "bias"))
+    out = torch.full((M, N), float("nan"), dtype=torch.float16 if half else torch.bfloat16,
+                     device="cuda")
     la = d["lora_act_in"] if R > 0 else None
     lu = d["lora_up"] if R > 0 else None
     binding.svdq_w4a4_gemm(d["act"], d["wgt"], d["ascales"], d["wscales"], la, lu,

@@ -87,7 +87,8 @@ def call(lib, M=256, N=256, K=256, R=32, ptrs=None, opts=None):
     (dict(opts=dict(stages=1)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(stages=9)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(debug_fault=2)), binding.SVDQ_ERR_BAD_OPTION),
-    (dict(opts=dict(reserved=(ctypes.c_int32 * 2)(0, 1))), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(reserved=1)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(io_dtype=2)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(cta_group=3)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(cta_group=2, tile_n=128)), binding.SVDQ_ERR_BAD_OPTION),
 ])
