@@ -1,7 +1,7 @@
 """Throughput of the W4A4 NVFP4 + LoRA linear operator on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--dense] [--fp16]
+                    [--workload NAME] [--dense] [--fp16] [--prepacked]
 
 One step is one operator call (the whole path: scale relayout, LoRA operand
 prep, LoRA + block-scaled MMAs, fused affine epilogue) over one synthetic
@@ -18,6 +18,8 @@ calibration variant of the workload: the same shape through the same kernel
 with R = 0 and no wcscale / bias, so the difference to the default run is
 the cost of the LoRA term and the affine epilogue.  `--fp16` runs the fp16
 input/output variant (lora_up, wcscale, bias and y in IEEE fp16).
+`--prepacked` prepacks the weights once before timing (packed scale words,
+LU' = LU / wcscale, as at weight-load time) and times the prepacked call.
 """
 
 from __future__ import annotations
@@ -51,6 +53,8 @@ def parse():
                     help="calibration variant: R = 0, no wcscale, no bias")
     ap.add_argument("--fp16", action="store_true",
                     help="fp16 input/output variant (lora_up, wcscale, bias, y in fp16)")
+    ap.add_argument("--prepacked", action="store_true",
+                    help="weights prepacked once (svdq_prepack_weights); time the prepacked call")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -246,6 +250,16 @@ def run_ours(args, w, rank, world, local_rank):
 
     inp = workload_inputs(synth, w, args.dense, args.fp16)
     d = {k: v.to(dev) for k, v in inp.items()}
+    if args.prepacked:
+        # once per weight load, outside every timed region
+        wpk, lup = pkg.svdq_prepack_weights(d["wscales"], d["lora_up"] if w.R else None,
+                                            d.get("wcscale"))
+        d = dict(d, wscales=wpk, lora_up=lup)
+        torch.cuda.synchronize(dev)
+    # what the end-to-end call copies from the host each step (the packed
+    # weights when prepacked)
+    host_src = {k: v.cpu() for k, v in d.items() if v is not None} if args.prepacked else inp
+    gemm = pkg.svdq_w4a4_gemm_prepacked if args.prepacked else pkg.svdq_w4a4_gemm
     out_dtype = torch.float16 if args.fp16 else torch.bfloat16
     out = torch.empty((w.M, w.N), dtype=out_dtype, device=dev)
     opts = dict(tile_n=args.tile_n, stages=args.stages)
@@ -253,9 +267,8 @@ def run_ours(args, w, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
 
     def step(o=out, dd=d):
-        pkg.svdq_w4a4_gemm(dd["act"], dd["wgt"], dd["ascales"], dd["wscales"], dd["lora_act_in"],
-                           dd["lora_up"], dd.get("wcscale"), dd.get("bias"), o, stream=stream,
-                           options=opts)
+        gemm(dd["act"], dd["wgt"], dd["ascales"], dd["wscales"], dd.get("lora_act_in"),
+             dd.get("lora_up"), dd.get("wcscale"), dd.get("bias"), o, stream=stream, options=opts)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(max(3, args.warmup)):
@@ -291,9 +304,9 @@ def run_ours(args, w, rank, world, local_rank):
         raise RuntimeError(f"device status {code} at wait site {site} in the timed region")
 
     # end to end through the public call: pinned host inputs -> device -> op -> host
-    host = {k: v.pin_memory() for k, v in inp.items()}
+    host = {k: v.pin_memory() for k, v in host_src.items()}
     host_out = torch.empty((w.M, w.N), dtype=out_dtype).pin_memory()
-    dd = {k: torch.empty_like(v, device=dev) for k, v in inp.items()}
+    dd = {k: torch.empty_like(v, device=dev) for k, v in host_src.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = host_out.numel() * host_out.element_size()
     e_ms = []
@@ -370,13 +383,15 @@ def main():
     from nvfp4_w4a4_quantized_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
-    if args.dense or args.fp16:
+    if args.dense or args.fp16 or args.prepacked:
         import dataclasses
 
         if args.dense:
             w = dataclasses.replace(w, name=w.name + "_dense", R=0)
         if args.fp16:
             w = dataclasses.replace(w, name=w.name + "_fp16")
+        if args.prepacked:
+            w = dataclasses.replace(w, name=w.name + "_prepacked")
     if args.impl == "reference":
         run_reference(args, w, rank)
     else:

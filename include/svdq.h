@@ -115,6 +115,51 @@ int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* ascales, con
                       const void* bias, void* out, int64_t M, int64_t N, int64_t K, int64_t R,
                       const svdq_options_t* options, void* stream);
 
+/*
+ * svdq_prepack_weights -- the weight-side operands in the form the kernel
+ * consumes them, built once per weight load ("SVDQuant W4A4 on Blackwell"
+ * §3.1: the tensor core takes the four group scales of one 64-wide K step
+ * as one 32-bit word per row; §6.3: the LoRA up-projection shares the main
+ * accumulator, so it is pre-divided by wcscale).  Weights are static, so
+ * neither the per-call scale transpose nor the divide needs to be repeated.
+ *
+ * wscales        device, uint8 [K/16, N] FP8-E4M3 (as for svdq_w4a4_gemm).
+ * lora_up        device, 16-bit [N, R]; NULL if and only if R == 0.
+ * wcscale        device, 16-bit [N]; NULL means 1.
+ * N, K, R        as for svdq_w4a4_gemm (N a multiple of 16, K of 64, R <= 128).
+ * io_dtype       SVDQ_IO_BF16 or SVDQ_IO_FP16: the type of lora_up, wcscale
+ *                and lora_up_packed.
+ * wscales_packed device, uint32 [K/64, N] (K*N/16 bytes, the same size as
+ *                wscales): word (s, n) holds byte g (bits 8g..8g+7) =
+ *                wscales[4s + g][n], g < 4.
+ * lora_up_packed device, 16-bit [N, R]: LU'[n][r] = round16(fp32(lora_up[n][r])
+ *                * rcp(wcscale[n])) with the correctly rounded fp32 reciprocal,
+ *                one fp32 product and round-to-nearest-even into io_dtype;
+ *                0 where wcscale[n] == 0, lora_up itself when wcscale is NULL.
+ *                Ignored (may be NULL) when R == 0.
+ * stream         a cudaStream_t.
+ *
+ * Every pointer must be 16-byte aligned; outputs must not overlap inputs.
+ * Asynchronous on `stream`, allocates nothing.  Returns SVDQ_OK for N == 0.
+ */
+int svdq_prepack_weights(const void* wscales, const void* lora_up, const void* wcscale,
+                         int64_t N, int64_t K, int64_t R, int32_t io_dtype, void* wscales_packed,
+                         void* lora_up_packed, void* stream);
+
+/*
+ * svdq_w4a4_gemm_prepacked -- svdq_w4a4_gemm_ex on prepacked weights: the
+ * same operator and result, with wscales_packed and lora_up_packed from
+ * svdq_prepack_weights in place of wscales and lora_up.  wcscale must be the
+ * one the LoRA operand was packed with (the epilogue still multiplies by it);
+ * bias, options and every other argument are as for svdq_w4a4_gemm_ex
+ * (options->io_dtype must match the packing).
+ */
+int svdq_w4a4_gemm_prepacked(const void* act, const void* wgt, const void* ascales,
+                             const void* wscales_packed, const float* lora_act_in,
+                             const void* lora_up_packed, const void* wcscale, const void* bias,
+                             void* out, int64_t M, int64_t N, int64_t K, int64_t R,
+                             const svdq_options_t* options, void* stream);
+
 /* The launch plan the library would use (host only; touches no device when
  * sm_count > 0).  Shared-memory accounting follows "SVDQuant W4A4 on
  * Blackwell" §7 (pipeline depth solved from the per-SM budget after every

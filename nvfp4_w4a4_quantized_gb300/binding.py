@@ -29,7 +29,8 @@ SVDQ_IO_BF16 = 0
 SVDQ_IO_FP16 = 1
 
 # Every symbol include/svdq.h declares.
-EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_query_plan", "svdq_lora_stage_bytes",
+EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_prepack_weights",
+            "svdq_w4a4_gemm_prepacked", "svdq_query_plan", "svdq_lora_stage_bytes",
             "svdq_read_device_status", "svdq_status_string", "svdq_version")
 
 
@@ -86,6 +87,11 @@ def load(path: Optional[str] = None):
         lib.svdq_w4a4_gemm.argtypes = [vp] * 9 + [i64] * 4 + [vp]
         lib.svdq_w4a4_gemm_ex.restype = ctypes.c_int
         lib.svdq_w4a4_gemm_ex.argtypes = [vp] * 9 + [i64] * 4 + [ctypes.POINTER(SvdqOptions), vp]
+        lib.svdq_prepack_weights.restype = ctypes.c_int
+        lib.svdq_prepack_weights.argtypes = [vp] * 3 + [i64] * 3 + [i32] + [vp] * 3
+        lib.svdq_w4a4_gemm_prepacked.restype = ctypes.c_int
+        lib.svdq_w4a4_gemm_prepacked.argtypes = ([vp] * 9 + [i64] * 4 +
+                                                 [ctypes.POINTER(SvdqOptions), vp])
         lib.svdq_query_plan.restype = ctypes.c_int
         lib.svdq_query_plan.argtypes = [i64] * 4 + [ctypes.POINTER(SvdqOptions), i32,
                                                     ctypes.POINTER(SvdqPlan)]
@@ -135,6 +141,12 @@ def _stream_handle(stream, device) -> int:
     return stream.cuda_stream
 
 
+def _check(name, t, dt):
+    if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous CUDA {dt}, got {t.dtype} "
+                         f"on {t.device} (contiguous={t.is_contiguous()})")
+
+
 def svdq_w4a4_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out,
                    stream=None, options=None, check: bool = True) -> int:
     """y = scaled_mma(act4, wgt4) * wcscale + bias + lora_act_in @ lora_up into ``out``.
@@ -148,6 +160,22 @@ def svdq_w4a4_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bi
     ``stream`` (default: torch's current stream).  Raises SvdqError on a
     non-zero status when ``check``; returns the status otherwise.
     """
+    return _gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, stream,
+                 options, check, prepacked=False)
+
+
+def svdq_w4a4_gemm_prepacked(act, wgt, ascales, wscales_packed, lora_act_in, lora_up_packed,
+                             wcscale, bias, out, stream=None, options=None,
+                             check: bool = True) -> int:
+    """svdq_w4a4_gemm on prepacked weights (see svdq_prepack_weights):
+    wscales_packed int32 [K/64, N] scale words, lora_up_packed LU' [N, R];
+    ``wcscale`` must be the one LU' was packed with."""
+    return _gemm(act, wgt, ascales, wscales_packed, lora_act_in, lora_up_packed, wcscale, bias,
+                 out, stream, options, check, prepacked=True)
+
+
+def _gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, stream, options,
+          check, prepacked):
     import torch
 
     M, kh = act.shape
@@ -155,18 +183,17 @@ def svdq_w4a4_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bi
     K = 2 * kh
     R = 0 if lora_act_in is None else int(lora_act_in.shape[1])
     h16 = torch.float16 if out.dtype == torch.float16 else torch.bfloat16
+    ws_dt = torch.int32 if prepacked else torch.uint8
+    ws_shape = (K // 64, N) if prepacked else (K // 16, N)
     for name, t, dt in (("act", act, torch.uint8), ("wgt", wgt, torch.uint8),
-                        ("ascales", ascales, torch.uint8), ("wscales", wscales, torch.uint8),
+                        ("ascales", ascales, torch.uint8), ("wscales", wscales, ws_dt),
                         ("lora_act_in", lora_act_in, torch.float32),
                         ("lora_up", lora_up if R else None, h16), ("wcscale", wcscale, h16),
                         ("bias", bias, h16), ("out", out, h16)):
-        if t is None:
-            continue
-        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name}: expected contiguous CUDA {dt}, got {t.dtype} "
-                             f"on {t.device} (contiguous={t.is_contiguous()})")
+        if t is not None:
+            _check(name, t, dt)
     if tuple(wgt.shape) != (N, kh) or tuple(ascales.shape) != (K // 16, M) or \
-            tuple(wscales.shape) != (K // 16, N) or tuple(out.shape) != (M, N):
+            tuple(wscales.shape) != ws_shape or tuple(out.shape) != (M, N):
         raise ValueError("inconsistent operand shapes")
     if R and (lora_up is None or tuple(lora_up.shape) != (N, R)):
         raise ValueError("lora_up must be [N, R]")
@@ -182,13 +209,59 @@ def svdq_w4a4_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bi
     args = [_ptr(act), _ptr(wgt), _ptr(ascales), _ptr(wscales), _ptr(lora_act_in),
             _ptr(lora_up), _ptr(wcscale), _ptr(bias), _ptr(out), M, N, K, R]
     with torch.cuda.device(act.device):
-        if opts is None:
+        if prepacked:
+            rc = lib.svdq_w4a4_gemm_prepacked(*args, ctypes.byref(opts) if opts else None, h)
+        elif opts is None:
             rc = lib.svdq_w4a4_gemm(*args, h)
         else:
             rc = lib.svdq_w4a4_gemm_ex(*args, ctypes.byref(opts), h)
     if check and rc != SVDQ_OK:
-        raise SvdqError(rc, "svdq_w4a4_gemm")
+        raise SvdqError(rc, "svdq_w4a4_gemm_prepacked" if prepacked else "svdq_w4a4_gemm")
     return rc
+
+
+def svdq_prepack_weights(wscales, lora_up, wcscale, wscales_packed=None, lora_up_packed=None,
+                         stream=None, check: bool = True):
+    """Weight-side prepack on the GPU: returns (wscales_packed int32 [K/64, N],
+    lora_up_packed [N, R] or None).  Output tensors are allocated here unless
+    given.  lora_up / wcscale are bf16, or fp16 for the fp16 variant."""
+    import torch
+
+    G, N = wscales.shape
+    K = 16 * G
+    R = 0 if lora_up is None else int(lora_up.shape[1])
+    h16 = lora_up.dtype if lora_up is not None else (
+        wcscale.dtype if wcscale is not None else torch.bfloat16)
+    if h16 not in (torch.bfloat16, torch.float16):
+        raise ValueError("lora_up / wcscale must be bf16 or fp16")
+    _check("wscales", wscales, torch.uint8)
+    if lora_up is not None:
+        _check("lora_up", lora_up, h16)
+        if tuple(lora_up.shape) != (N, R):
+            raise ValueError("lora_up must be [N, R]")
+    if wcscale is not None:
+        _check("wcscale", wcscale, h16)
+        if tuple(wcscale.shape) != (N,):
+            raise ValueError("wcscale must be [N]")
+    if K % 64:
+        raise ValueError("K must be a multiple of 64")
+    if wscales_packed is None:
+        wscales_packed = torch.empty((K // 64, N), dtype=torch.int32, device=wscales.device)
+    _check("wscales_packed", wscales_packed, torch.int32)
+    if R and lora_up_packed is None:
+        lora_up_packed = torch.empty((N, R), dtype=h16, device=wscales.device)
+    if R:
+        _check("lora_up_packed", lora_up_packed, h16)
+    io = SVDQ_IO_FP16 if h16 == torch.float16 else SVDQ_IO_BF16
+    lib = load()
+    h = _stream_handle(stream, wscales.device)
+    with torch.cuda.device(wscales.device):
+        rc = lib.svdq_prepack_weights(_ptr(wscales), _ptr(lora_up) if R else None,
+                                      _ptr(wcscale), N, K, R, io, _ptr(wscales_packed),
+                                      _ptr(lora_up_packed) if R else None, h)
+    if check and rc != SVDQ_OK:
+        raise SvdqError(rc, "svdq_prepack_weights")
+    return wscales_packed, (lora_up_packed if R else None)
 
 
 def svdq_query_plan(M: int, N: int, K: int, R: int, options=None, sm_count: int = 0) -> dict:

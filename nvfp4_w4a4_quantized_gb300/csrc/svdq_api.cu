@@ -13,6 +13,7 @@
 
 #include "svdq.h"
 #include "svdq_kernel.cuh"
+#include "svdq_prepack.cuh"
 
 namespace svdq {
 
@@ -341,12 +342,22 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
     if ((rc = encode(&tm[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.ascales, d_sfa, s_sfa, b_sfa,
                      CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
       return rc;
-    const uint64_t d_sfb[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K / 16)},
-                   s_sfb[1] = {static_cast<uint64_t>(N)};
-    const uint32_t b_sfb[2] = {BN, 16 * KBI};
-    if ((rc = encode(&tm[3], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.wscales, d_sfb, s_sfb, b_sfb,
-                     CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
-      return rc;
+    if (kp.prepacked) {
+      // packed scale words uint32 [K/64][N]: the same 16 * BN bytes per K block
+      const uint64_t d_sfb[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K / 64)},
+                     s_sfb[1] = {static_cast<uint64_t>(N) * 4};
+      const uint32_t b_sfb[2] = {BN, 4 * KBI};
+      if ((rc = encode(&tm[3], CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, op.wscales, d_sfb, s_sfb,
+                       b_sfb, CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
+        return rc;
+    } else {
+      const uint64_t d_sfb[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K / 16)},
+                     s_sfb[1] = {static_cast<uint64_t>(N)};
+      const uint32_t b_sfb[2] = {BN, 16 * KBI};
+      if ((rc = encode(&tm[3], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.wscales, d_sfb, s_sfb, b_sfb,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
+        return rc;
+    }
     // output: one store writes rows 4a + q (a < 32) of a 128-row block
     const uint64_t d_out[3] = {static_cast<uint64_t>(N), M4, 4},
                    s_out[2] = {static_cast<uint64_t>(N) * 8, static_cast<uint64_t>(N) * 2};
@@ -402,16 +413,12 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-}  // namespace
-}  // namespace svdq
-
-using namespace svdq;
-
-extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* ascales,
-                                 const void* wscales, const float* lora_act_in,
-                                 const void* lora_up, const void* wcscale, const void* bias,
-                                 void* out, int64_t M, int64_t N, int64_t K, int64_t R,
-                                 const svdq_options_t* options, void* stream) {
+// One operator call; `prepacked` selects packed scale words and LU' (from
+// svdq_prepack_weights) for wscales / lora_up.
+int run_gemm(const void* act, const void* wgt, const void* ascales, const void* wscales,
+             const float* lora_act_in, const void* lora_up, const void* wcscale, const void* bias,
+             void* out, int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* options,
+             void* stream, bool prepacked) {
   int rc = validate_options(options);
   if (rc != SVDQ_OK) return rc;
   const bool f16 = options != nullptr && options->io_dtype == SVDQ_IO_FP16;
@@ -462,6 +469,7 @@ extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* a
   kp.r16 = pl.r16;
   kp.num_stages = pl.stages;
   kp.lora_tma = (R > 0 && R % 8 == 0);
+  kp.prepacked = prepacked ? 1 : 0;
   kp.debug_fault = options ? options->debug_fault : 0;
   const int tmo = (options && options->timeout_ms) ? options->timeout_ms : kDefaultTimeoutMs;
   kp.timeout_ns = static_cast<unsigned long long>(tmo) * 1000000ull;
@@ -481,6 +489,69 @@ extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* a
   if (pl.cta_group == 2) return launch<2, 256, false>(pl, dinfo, op, kp, M, N, K, R, s);
   if (pl.tile_n == 256) return launch<1, 256, false>(pl, dinfo, op, kp, M, N, K, R, s);
   return launch<1, 128, false>(pl, dinfo, op, kp, M, N, K, R, s);
+}
+
+}  // namespace
+}  // namespace svdq
+
+using namespace svdq;
+
+extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* ascales,
+                                 const void* wscales, const float* lora_act_in,
+                                 const void* lora_up, const void* wcscale, const void* bias,
+                                 void* out, int64_t M, int64_t N, int64_t K, int64_t R,
+                                 const svdq_options_t* options, void* stream) {
+  return run_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, M, N, K,
+                  R, options, stream, false);
+}
+
+extern "C" int svdq_w4a4_gemm_prepacked(const void* act, const void* wgt, const void* ascales,
+                                        const void* wscales_packed, const float* lora_act_in,
+                                        const void* lora_up_packed, const void* wcscale,
+                                        const void* bias, void* out, int64_t M, int64_t N,
+                                        int64_t K, int64_t R, const svdq_options_t* options,
+                                        void* stream) {
+  return run_gemm(act, wgt, ascales, wscales_packed, lora_act_in, lora_up_packed, wcscale, bias,
+                  out, M, N, K, R, options, stream, true);
+}
+
+extern "C" int svdq_prepack_weights(const void* wscales, const void* lora_up,
+                                    const void* wcscale, int64_t N, int64_t K, int64_t R,
+                                    int32_t io_dtype, void* wscales_packed,
+                                    void* lora_up_packed, void* stream) {
+  if (io_dtype != SVDQ_IO_BF16 && io_dtype != SVDQ_IO_FP16) return SVDQ_ERR_BAD_OPTION;
+  if (N < 0 || K <= 0 || R < 0) return SVDQ_ERR_INVALID_ARG;
+  if (N % 16 || K % 64 || N > SVDQ_MAX_MN || K > SVDQ_MAX_K || R > SVDQ_MAX_RANK)
+    return SVDQ_ERR_UNSUPPORTED_SHAPE;
+  if (!wscales || !wscales_packed) return SVDQ_ERR_INVALID_ARG;
+  if (R > 0 && (!lora_up || !lora_up_packed)) return SVDQ_ERR_INVALID_ARG;
+  const void* ptrs[] = {wscales, wscales_packed, lora_up, lora_up_packed, wcscale};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return SVDQ_ERR_MISALIGNED;
+  if (N == 0) return SVDQ_OK;
+  int dev = 0;
+  DeviceInfo* dinfo = nullptr;
+  int rc = probe_device(&dev, &dinfo);
+  if (rc != SVDQ_OK) return rc;
+  const long long work = (K / 64) * (N / 4) + N * R;
+  long long blocks = (work + 255) / 256;
+  const long long cap = 8LL * dinfo->sm_count;
+  if (blocks > cap) blocks = cap;
+  const uint8_t* ws = static_cast<const uint8_t*>(wscales);
+  const uint16_t* lu = R > 0 ? static_cast<const uint16_t*>(lora_up) : nullptr;
+  const uint16_t* wc = static_cast<const uint16_t*>(wcscale);
+  uint32_t* wpk = static_cast<uint32_t*>(wscales_packed);
+  uint16_t* lup = R > 0 ? static_cast<uint16_t*>(lora_up_packed) : nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int n = static_cast<int>(N), k = static_cast<int>(K), r = static_cast<int>(R);
+  if (io_dtype == SVDQ_IO_FP16)
+    svdq_prepack_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(ws, lu, wc, wpk, lup,
+                                                                             n, k, r);
+  else
+    svdq_prepack_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(ws, lu, wc, wpk,
+                                                                              lup, n, k, r);
+  if (cudaGetLastError() != cudaSuccess) return SVDQ_ERR_LAUNCH;
+  return SVDQ_OK;
 }
 
 extern "C" int svdq_w4a4_gemm(const void* act, const void* wgt, const void* ascales,
@@ -581,4 +652,4 @@ extern "C" const char* svdq_status_string(int status) {
   }
 }
 
-extern "C" int svdq_version(void) { return 100; }
+extern "C" int svdq_version(void) { return 200; }

@@ -26,36 +26,41 @@
 // row order (warp q's lane a is output row 4a + q) and its columns the B order
 // (column 128h + a + 32b is output column 128h + 4a + b).
 //
-// 14 warps per CTA:
+// 15 warps per CTA (480 threads):
 //   warps 0, 12, 13  TMA producers, one thread each, every ring item split
 //                three ways (one issuing thread streams far fewer bytes per
-//                second than three): warp 0 the raw [16 groups x rows] scale
+//                second than three): warp 0 the [16 groups x rows] scale
 //                boxes, the LoRA item rows and the leader's byte count; warp 12
 //                the packed act tiles; warp 13 the packed wgt tiles (128-byte
-//                swizzle).  LoRA ring item (32 ranks): raw fp32 LA rows, bf16
+//                swizzle).  LoRA ring item (32 ranks): raw fp32 LA rows, 16-bit
 //                LU rows (64-byte swizzle) and wcscale.
-//   warp 1       MMA issuer (one thread, leader CTA): tcgen05.mma kind::mxf4nvf4
-//                block_scale.scale_vec::4X for main items, kind::f16 (bf16) for
-//                LoRA items, commits that free ring stages / publish accumulators.
-//   warps 2, 3   LoRA operand builders: LU' = bf16(LU / wc), half the rows each,
-//                written into the stage in the MMA's K-major 64-byte-swizzle layout
-//                (the scale feeders build LA' = bf16(LA), 32 rows each).
-//   warps 4..7   epilogue: tcgen05.ld (64 columns at a time) -> fma(acc, wc, bias)
-//                -> bf16 -> shared staging (128-byte swizzle) -> TMA tile store;
-//                the accumulator is released as soon as its last columns are
-//                in registers.
-//   warps 8..11  scale feeders: transpose the stage's raw scale boxes into
-//                row-per-lane words in registers and write them into tensor
-//                memory with tcgen05.st (one warp per 32-lane quadrant), off
-//                the MMA pipe.
+//   warps 1, 14  MMA issuers (one thread each, leader CTA), alternating ring
+//                items: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X for
+//                main items, kind::f16 (bf16 or fp16) for LoRA items, commits
+//                that free ring stages / publish accumulators.
+//   warps 2, 3   LoRA operand builders: LU' = round16(LU / wc), half the rows
+//                each, in place in the stage's K-major 64-byte-swizzle layout
+//                (nothing to do for prepacked weights, whose LU' arrives ready).
+//   warps 4..7   epilogue: tcgen05.ld (32 columns at a time, software-
+//                pipelined) -> fma(acc, wc, bias) -> 16-bit -> shared staging
+//                (128-byte swizzle) -> TMA tile store; every column read is
+//                cleared for the next tile and the accumulator released after
+//                the last one.
+//   warps 8..11  scale feeders: turn the stage's scale boxes into row-per-lane
+//                words in registers (a 4x4 byte transpose of raw scales, or
+//                plain 16-byte loads of prepacked weight-scale words) and write
+//                them into tensor memory with tcgen05.st (one warp per 32-lane
+//                quadrant), off the MMA pipe; on LoRA items they build
+//                LA' = round16(LA), 32 rows each.
 // Warp 4+q / 8+q own tensor-memory lanes 32q .. 32q+31.
 //
 // Per output tile the ring carries ceil(R/32) LoRA items, then ceil(K/256)
 // main items; every role walks the same item sequence, so stage index and
-// phase bit survive tile boundaries.  LoRA MMAs run first (the first one
-// overwrites the accumulator); one commit+wait orders them before the
-// block-scaled MMAs of another kind.  LU' is pre-divided by wcscale, so the
-// epilogue's acc * wcscale restores LA @ LU unscaled, as the operator states.
+// phase bit survive tile boundaries.  Every MMA accumulates into an
+// accumulator the epilogue has cleared, so the LoRA and block-scaled MMAs of
+// the two issuers may reach the tensor core in any order.  LU' is pre-divided
+// by wcscale, so the epilogue's acc * wcscale restores LA @ LU unscaled, as the
+// operator states.
 //
 // Every mbarrier wait is bounded by %globaltimer; on expiry the kernel records
 // SVDQ_ERR_TIMEOUT and the wait site, every role leaves its loop, in-flight
@@ -67,6 +72,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -160,6 +166,7 @@ struct KParams {
   int r16;          // R rounded up to 16
   int num_stages;
   int lora_tma;     // R % 8 == 0: LoRA rows arrive by TMA; else direct loads
+  int prepacked;    // weights prepacked: scale words [K/64][N], lora_up = LU'
   int debug_fault;
   unsigned long long timeout_ns;
   const float* lora_act_in;
@@ -386,13 +393,14 @@ __device__ __forceinline__ void lora_la_direct(uint8_t* dst, const KParams& p, i
   }
 }
 
+// `wc` is NULL for a prepacked LU' (already divided) or an absent wcscale.
 template <int NR, bool F16>
-__device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p, int n_cta, int blk,
-                                               int r0, int lane) {
+__device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p,
+                                               const uint16_t* wc, int n_cta, int blk, int r0,
+                                               int lane) {
   const int chunk = lane & 3;
   const int k0 = blk * kLoraRanks + chunk * 8;
   const uint16_t* lu = p.lora_up;
-  const uint16_t* wc = p.wcscale;
   for (int it = 0; it < NR / 8; ++it) {
     const int row = r0 + it * 8 + (lane >> 2);
     const int n = n_cta + quad_row(row);
@@ -506,8 +514,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       const uint32_t main_aux_bytes = 16 * KBI * (kBM + BN);
+      // the LoRA item stages wcscale only to divide LU by it in place
+      const bool stage_wc = p.wcscale != nullptr && !p.prepacked;
       const uint32_t lora_aux_bytes =
-          kBM * kLoraRanks * 4 + L::kBNc * 64 + (p.wcscale != nullptr ? 2 * L::kBNc : 0);
+          kBM * kLoraRanks * 4 + L::kBNc * 64 + (stage_wc ? 2 * L::kBNc : 0);
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
         int mb, nb;
         tile_coords(p, t, mb, nb);
@@ -538,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < L::kBNc / 128; ++h)
                   ptx::tma_load_3d(st + L::kLoraLU + 8192 * h, &tm_lu, ab, kLoraRanks * i,
                                    (n_cta + 128 * h) / 4, 0);
-                if (p.wcscale != nullptr) ptx::tma_load_1d(st + L::kLoraWC, &tm_wc, ab, n_cta);
+                if (stage_wc) ptx::tma_load_1d(st + L::kLoraWC, &tm_wc, ab, n_cta);
               } else {
                 ptx::mbar_arrive(ab);
               }
@@ -550,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (role == 0) {
               ptx::mbar_arrive_expect_tx(ab, main_aux_bytes);
               ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, ab, m_cta, kb0 * 16);
-              ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, ab, n0, kb0 * 16);
+              // raw scales: 16 group rows per K block; packed words: 4 step rows
+              ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, ab, n0, kb0 * (p.prepacked ? 4 : 16));
               // The act / wgt loads of this item may land before this count
               // (the transaction count runs negative meanwhile); the phase
               // cannot complete before this arrival.
@@ -739,8 +750,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + stage * L::kStageBytes;
           const int r0 = (warp - 2) * (L::kBNc / 2);
           if (!p.lora_tma)
-            lora_lu_direct<L::kBNc / 2, F16>(st + L::kLoraLU, p, n_cta, i, r0, lane);
-          else if (p.wcscale != nullptr)
+            lora_lu_direct<L::kBNc / 2, F16>(st + L::kLoraLU, p,
+                                             p.prepacked ? nullptr : p.wcscale, n_cta, i, r0,
+                                             lane);
+          else if (p.wcscale != nullptr && !p.prepacked)
             lora_lu_scale_smem<L::kBNc / 2, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N,
                                                  r0, lane);
           ptx::fence_proxy_async_smem();
@@ -910,37 +923,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the block-scaled MMA reads the scale words in every quadrant.
           const uint32_t col = tmem_base + lane_base +
                                static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
+          // Prepacked weight scales arrive as words [step][BN]: lane a's four
+          // words of a 128-column half are 16 consecutive bytes.
+          auto feed = [&](auto packed_tag) {
+            constexpr bool kPacked = decltype(packed_tag)::value;
 #pragma unroll
-          for (int kk = 0; kk < KBI; ++kk) {
-            uint32_t a[16], b[16 * L::kSfbHalves];
+            for (int kk = 0; kk < KBI; ++kk) {
+              uint32_t a[16], b[16 * L::kSfbHalves];
 #pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) {
-              const int ks = 4 * kk + s4;
-              sf_words(st + L::kOffSFA + 4 * kBM * ks, kBM, lane, a + 4 * s4);
+              for (int s4 = 0; s4 < 4; ++s4) {
+                const int ks = 4 * kk + s4;
+                sf_words(st + L::kOffSFA + 4 * kBM * ks, kBM, lane, a + 4 * s4);
 #pragma unroll
-              for (int h = 0; h < L::kSfbHalves; ++h)
-                sf_words(st + L::kOffSFB + 4 * BN * ks + 128 * h, BN, lane,
-                         b + 4 * (s4 * L::kSfbHalves + h));
-            }
-            if (KBI == 1 && L::kSfbHalves == 2) {
-              // one K block: SFA (16 columns) and SFB (32) are adjacent; two
-              // stores instead of three (each store briefly holds up the MMAs)
-              uint32_t v[32];
-#pragma unroll
-              for (int x = 0; x < 16; ++x) {
-                v[x] = a[x];
-                v[16 + x] = b[x];
+                for (int h = 0; h < L::kSfbHalves; ++h) {
+                  uint32_t* bw = b + 4 * (s4 * L::kSfbHalves + h);
+                  if (kPacked) {
+                    const uint4 v =
+                        lds128(st + L::kOffSFB + 4 * BN * ks + 4 * (128 * h + 4 * lane));
+                    bw[0] = v.x;
+                    bw[1] = v.y;
+                    bw[2] = v.z;
+                    bw[3] = v.w;
+                  } else {
+                    sf_words(st + L::kOffSFB + 4 * BN * ks + 128 * h, BN, lane, bw);
+                  }
+                }
               }
-              ptx::tmem_st_32x32b_x32(col, v);
-              ptx::tmem_st_32x32b_x16(col + 32, b + 16);
-            } else {
-              ptx::tmem_st_32x32b_x16(col + 16 * kk, a);
+              if (KBI == 1 && L::kSfbHalves == 2) {
+                // one K block: SFA (16 columns) and SFB (32) are adjacent; two
+                // stores instead of three (each store briefly holds up the MMAs)
+                uint32_t v[32];
 #pragma unroll
-              for (int h = 0; h < L::kSfbHalves; ++h)
-                ptx::tmem_st_32x32b_x16(col + 4 * L::kSteps + 16 * L::kSfbHalves * kk + 16 * h,
-                                        b + 16 * h);
+                for (int x = 0; x < 16; ++x) {
+                  v[x] = a[x];
+                  v[16 + x] = b[x];
+                }
+                ptx::tmem_st_32x32b_x32(col, v);
+                ptx::tmem_st_32x32b_x16(col + 32, b + 16);
+              } else {
+                ptx::tmem_st_32x32b_x16(col + 16 * kk, a);
+#pragma unroll
+                for (int h = 0; h < L::kSfbHalves; ++h)
+                  ptx::tmem_st_32x32b_x16(col + 4 * L::kSteps + 16 * L::kSfbHalves * kk + 16 * h,
+                                          b + 16 * h);
+              }
             }
-          }
+          };
+          if (p.prepacked)
+            feed(std::true_type{});
+          else
+            feed(std::false_type{});
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
         }

@@ -69,3 +69,29 @@ def sample_rows(M, count=48, seed=0):
 
 def oracle_y(inp, M, N, K, R, rows=None):
     return oracle.forward(inp, M, N, K, R, rows=rows)
+
+
+def prepack_gpu(inp, R):
+    """Prepack the weight side of `inp` (CPU tensors) on the GPU; returns the
+    device inputs with wscales / lora_up replaced by their packed forms."""
+    d = to_device(inp)
+    wpk, lup = binding.svdq_prepack_weights(d["wscales"], d["lora_up"] if R > 0 else None,
+                                            d.get("wcscale"))
+    return dict(d, wscales=wpk, lora_up=lup)
+
+
+def run_gpu_prepacked(inp, M, N, K, R, options=None):
+    """The prepacked route: svdq_prepack_weights, then svdq_w4a4_gemm_prepacked
+    (both on the GPU); y as float64 numpy."""
+    d = prepack_gpu(inp, R)
+    half = any(isinstance(inp.get(k), torch.Tensor) and inp[k].dtype == torch.float16
+               for k in ("lora_up", "wcscale", "bias"))
+    out = torch.full((M, N), float("nan"), dtype=torch.float16 if half else torch.bfloat16,
+                     device="cuda")
+    binding.svdq_w4a4_gemm_prepacked(d["act"], d["wgt"], d["ascales"], d["wscales"],
+                                     d["lora_act_in"] if R > 0 else None, d["lora_up"],
+                                     d.get("wcscale"), d.get("bias"), out, options=options)
+    torch.cuda.synchronize()
+    code, site, block = binding.svdq_read_device_status(clear=True)
+    assert code == 0, f"device status {code} at wait site {site}, CTA {block}"
+    return out.to(torch.float64).cpu().numpy()

@@ -47,18 +47,21 @@ def test_status_strings(lib):
         s = binding.status_string(code)
         assert s.startswith("SVDQ_")
     assert binding.status_string(-99) == "SVDQ_ERR_UNKNOWN"
-    assert binding.svdq_version() >= 100
+    assert binding.svdq_version() >= 200
 
 
 # ---------------------------------------------------------------- validation
 A = 1 << 20  # fake, 16-byte aligned addresses: validation never dereferences
 
 
-def call(lib, M=256, N=256, K=256, R=32, ptrs=None, opts=None):
+def call(lib, M=256, N=256, K=256, R=32, ptrs=None, opts=None, prepacked=False):
     p = dict(act=A, wgt=A, ascales=A, wscales=A, la=A, lu=A, wc=A, bias=A, out=A)
     p.update(ptrs or {})
     args = [p["act"], p["wgt"], p["ascales"], p["wscales"], p["la"], p["lu"], p["wc"], p["bias"],
             p["out"], M, N, K, R]
+    if prepacked:
+        o = binding.SvdqOptions(**(opts or {}))
+        return lib.svdq_w4a4_gemm_prepacked(*args, ctypes.byref(o) if opts else None, None)
     if opts is None:
         return lib.svdq_w4a4_gemm(*args, None)
     o = binding.SvdqOptions(**opts)
@@ -92,8 +95,43 @@ def call(lib, M=256, N=256, K=256, R=32, ptrs=None, opts=None):
     (dict(opts=dict(cta_group=3)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(cta_group=2, tile_n=128)), binding.SVDQ_ERR_BAD_OPTION),
 ])
-def test_host_validation(lib, kw, expect):
-    assert call(lib, **kw) == expect
+@pytest.mark.parametrize("prepacked", [False, True], ids=["per_call", "prepacked"])
+def test_host_validation(lib, kw, expect, prepacked):
+    assert call(lib, prepacked=prepacked, **kw) == expect
+
+
+def prepack(lib, N=256, K=256, R=32, io=0, ptrs=None):
+    p = dict(ws=A, lu=A, wc=A, wpk=A, lup=A)
+    p.update(ptrs or {})
+    return lib.svdq_prepack_weights(p["ws"], p["lu"], p["wc"], N, K, R, io, p["wpk"], p["lup"],
+                                    None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(io=2), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(io=-1), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(N=-16), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(K=0), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(R=-1), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(N=40), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (dict(K=96), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (dict(R=129), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (dict(ptrs=dict(ws=None)), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(ptrs=dict(wpk=None)), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(ptrs=dict(lu=None)), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(ptrs=dict(lup=None)), binding.SVDQ_ERR_INVALID_ARG),
+    (dict(ptrs=dict(ws=A + 8)), binding.SVDQ_ERR_MISALIGNED),
+    (dict(ptrs=dict(lup=A + 2)), binding.SVDQ_ERR_MISALIGNED),
+    (dict(ptrs=dict(wc=A + 4)), binding.SVDQ_ERR_MISALIGNED),
+])
+def test_prepack_host_validation(lib, kw, expect):
+    assert prepack(lib, **kw) == expect
+
+
+def test_prepack_empty_and_rank_zero(lib):
+    assert prepack(lib, N=0) == binding.SVDQ_OK
+    # R == 0 needs no LoRA pointers (N == 0 keeps it off the device)
+    assert prepack(lib, N=0, R=0, ptrs=dict(lu=None, lup=None, wc=None)) == binding.SVDQ_OK
 
 
 def test_rank_zero_needs_no_lora_pointers(lib):
@@ -109,6 +147,8 @@ def test_empty_product_is_a_no_op(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_no_device_is_reported(lib):
     assert call(lib) == binding.SVDQ_ERR_UNSUPPORTED_DEVICE
+    assert call(lib, prepacked=True) == binding.SVDQ_ERR_UNSUPPORTED_DEVICE
+    assert prepack(lib) == binding.SVDQ_ERR_UNSUPPORTED_DEVICE
 
 
 # ---------------------------------------------------------------- planner
