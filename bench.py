@@ -1,7 +1,7 @@
 """Throughput of the W4A4 NVFP4 + LoRA linear operator on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--dense] [--fp16] [--prepacked]
+                    [--workload NAME] [--dense] [--fp16] [--prepacked] [--split]
 
 One step is one operator call (the whole path: scale relayout, LoRA operand
 prep, LoRA + block-scaled MMAs, fused affine epilogue) over one synthetic
@@ -20,6 +20,8 @@ the cost of the LoRA term and the affine epilogue.  `--fp16` runs the fp16
 input/output variant (lora_up, wcscale, bias and y in IEEE fp16).
 `--prepacked` prepacks the weights once before timing (packed scale words,
 LU' = LU / wcscale, as at weight-load time) and times the prepacked call.
+`--split` times the split-K entry point (workspace allocated once, before
+timing; the planner decides the split, e.g. on mlp_down_256x3072x12288_r128).
 """
 
 from __future__ import annotations
@@ -55,6 +57,8 @@ def parse():
                     help="fp16 input/output variant (lora_up, wcscale, bias, y in fp16)")
     ap.add_argument("--prepacked", action="store_true",
                     help="weights prepacked once (svdq_prepack_weights); time the prepacked call")
+    ap.add_argument("--split", action="store_true",
+                    help="time svdq_w4a4_gemm_split (planner-chosen split-K)")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -260,10 +264,19 @@ def run_ours(args, w, rank, world, local_rank):
     # weights when prepacked)
     host_src = {k: v.cpu() for k, v in d.items() if v is not None} if args.prepacked else inp
     gemm = pkg.svdq_w4a4_gemm_prepacked if args.prepacked else pkg.svdq_w4a4_gemm
+    if args.split:
+        wsz = pkg.svdq_workspace_size(w.M, w.N, w.K, w.R,
+                                      options=dict(io_dtype=1 if args.fp16 else 0))
+        workspace = torch.zeros(max(wsz, 256), dtype=torch.uint8, device=dev)
+
+        def gemm(*a, options=None, **kw):
+            return pkg.svdq_w4a4_gemm_split(*a, workspace, options=options,
+                                            weights_prepacked=args.prepacked, **kw)
     out_dtype = torch.float16 if args.fp16 else torch.bfloat16
     out = torch.empty((w.M, w.N), dtype=out_dtype, device=dev)
     opts = dict(tile_n=args.tile_n, stages=args.stages)
-    plan = pkg.svdq_query_plan(w.M, w.N, w.K, w.R, options=opts)
+    plan = pkg.svdq_query_plan(w.M, w.N, w.K, w.R,
+                               options=dict(opts, k_splits=-1) if args.split else opts)
     stream = torch.cuda.current_stream(dev)
 
     def step(o=out, dd=d):
@@ -351,7 +364,7 @@ def run_ours(args, w, rank, world, local_rank):
                        "l2": "flushed: 256 MiB memset before every timed launch",
                        "parallelism": f"replicas x{world} (independent problems, no collective)",
                        "tile": [plan["tile_m"], plan["tile_n"]], "stages": plan["num_ab_stage"],
-                       "grid": plan["grid"]},
+                       "grid": plan["grid"], "k_splits": plan["k_splits"]},
             "mfu_vs_10pf": tflops_kernel / BASELINE_PEAK_TFLOPS,
             "ms_per_step_min": min(ms), "ms_per_step_median": statistics.median(ms),
             "wall_s_timed_region": t_wall,
@@ -383,7 +396,7 @@ def main():
     from nvfp4_w4a4_quantized_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
-    if args.dense or args.fp16 or args.prepacked:
+    if args.dense or args.fp16 or args.prepacked or args.split:
         import dataclasses
 
         if args.dense:
@@ -392,6 +405,8 @@ def main():
             w = dataclasses.replace(w, name=w.name + "_fp16")
         if args.prepacked:
             w = dataclasses.replace(w, name=w.name + "_prepacked")
+        if args.split:
+            w = dataclasses.replace(w, name=w.name + "_split")
     if args.impl == "reference":
         run_reference(args, w, rank)
     else:

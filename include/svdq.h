@@ -36,6 +36,8 @@ extern "C" {
 #define SVDQ_ERR_CUDA -6               /* another CUDA runtime/driver call failed       */
 #define SVDQ_ERR_TIMEOUT -7            /* device status only: a bounded wait expired     */
 #define SVDQ_ERR_BAD_OPTION -8         /* an svdq_options_t field is out of range       */
+#define SVDQ_ERR_WORKSPACE -9          /* split-K needs a workspace: missing, smaller than
+                                          svdq_workspace_size, or not 256-byte aligned  */
 
 /* Size limits: M, N <= 2^24 and K <= 2^20 (elements). */
 #define SVDQ_MAX_MN (1LL << 24)
@@ -102,7 +104,10 @@ typedef struct svdq_options {
     int32_t io_dtype;    /* 16-bit I/O type of lora_up, wcscale, bias and out:
                             SVDQ_IO_BF16 (0, default) or SVDQ_IO_FP16 (1, IEEE
                             binary16; LoRA operands are then rounded to fp16) */
-    int32_t reserved;    /* must be zero                                            */
+    int32_t k_splits;    /* split-K: 0 = default (none on entry points without a
+                            workspace, the planner's choice on svdq_w4a4_gemm_split);
+                            -1 = the planner's choice; 1 = none; 2..8 = that many K
+                            splits per tile (svdq_w4a4_gemm_split only)           */
 } svdq_options_t;
 
 /* svdq_w4a4_gemm with options; identical semantics otherwise.  With
@@ -160,6 +165,46 @@ int svdq_w4a4_gemm_prepacked(const void* act, const void* wgt, const void* ascal
                              void* out, int64_t M, int64_t N, int64_t K, int64_t R,
                              const svdq_options_t* options, void* stream);
 
+/*
+ * svdq_w4a4_gemm_split -- the operator with split-K: each output tile's K
+ * range is divided into k_splits parts that run on different SMs at once;
+ * every part but the last writes an fp32 partial tile into `workspace`, the
+ * last adds them to its own accumulator and applies the epilogue.  This is
+ * for shapes whose tiles leave most SMs idle (few rows, e.g. M = 256) and
+ * whose K is long: the planner splits only when the tiles fill at most half
+ * of the co-resident clusters, gives every part a cluster of its own and
+ * keeps at least eight 256-wide K blocks per part (a split costs about as
+ * much as ten K blocks of tensor-core work).  Forced splits (k_splits 2..8)
+ * need at least one K block per part.  "SVDQuant W4A4 on Blackwell" §4 names the small-M
+ * case; the split itself is this library's.
+ *
+ * Arguments are those of svdq_w4a4_gemm_ex (or svdq_w4a4_gemm_prepacked when
+ * weights_prepacked == 1), plus:
+ * workspace        device, at least svdq_workspace_size(...) bytes, 256-byte
+ *                  aligned, zero-filled before its first use; owned by the
+ *                  caller and reused across calls.  Calls that share a
+ *                  workspace must not overlap on the GPU (they would race on
+ *                  its contents).
+ * workspace_bytes  its size.
+ * When the plan has no split the workspace is not touched.  The summation
+ * order of the K parts differs from the unsplit kernel (fp32 partials), so
+ * results agree with it within the operator's tolerance, not bit for bit.
+ * Returns SVDQ_ERR_WORKSPACE if the workspace is missing or too small.
+ */
+int svdq_w4a4_gemm_split(const void* act, const void* wgt, const void* ascales,
+                         const void* wscales, const float* lora_act_in, const void* lora_up,
+                         const void* wcscale, const void* bias, void* out, int64_t M, int64_t N,
+                         int64_t K, int64_t R, const svdq_options_t* options,
+                         int32_t weights_prepacked, void* workspace, int64_t workspace_bytes,
+                         void* stream);
+
+/* Workspace bytes svdq_w4a4_gemm_split needs for this shape and options
+ * (0 when the plan does not split), or a negative status.  sm_count <= 0
+ * plans exactly as a launch on the current device does; sm_count > 0 plans
+ * for that many SMs without touching a device. */
+int64_t svdq_workspace_size(int64_t M, int64_t N, int64_t K, int64_t R,
+                            const svdq_options_t* options, int32_t sm_count);
+
 /* The launch plan the library would use (host only; touches no device when
  * sm_count > 0).  Shared-memory accounting follows "SVDQuant W4A4 on
  * Blackwell" §7 (pipeline depth solved from the per-SM budget after every
@@ -181,12 +226,17 @@ typedef struct svdq_plan {
     int32_t grid;                    /* persistent CTAs launched                     */
     int32_t sm_count;                /* SMs the grid was sized for                   */
     int32_t kblocks_per_stage;       /* 256-wide K blocks carried by one ring stage  */
+    int32_t k_splits;                /* K splits per tile (1: none)                  */
+    int64_t num_units;               /* work units: num_tiles * k_splits             */
+    int64_t workspace_bytes;         /* split-K workspace the launch needs (0: none) */
 } svdq_plan_t;
 
 /* Fill *plan for the given shape.  sm_count <= 0 queries the current device
  * (SVDQ_ERR_UNSUPPORTED_DEVICE if none); sm_count > 0 plans for that many
  * SMs with GB300 limits (227 KB shared memory per block, 512 TMEM columns)
- * and touches no device. */
+ * and touches no device.  With options->k_splits == 0 the plan is that of the
+ * entry points without a workspace (no split-K); -1 or 2..8 plans split-K as
+ * svdq_w4a4_gemm_split would. */
 int svdq_query_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* options,
                     int32_t sm_count, svdq_plan_t* plan);
 

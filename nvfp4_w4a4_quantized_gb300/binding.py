@@ -24,21 +24,23 @@ SVDQ_ERR_LAUNCH = -5
 SVDQ_ERR_CUDA = -6
 SVDQ_ERR_TIMEOUT = -7
 SVDQ_ERR_BAD_OPTION = -8
+SVDQ_ERR_WORKSPACE = -9
 
 SVDQ_IO_BF16 = 0
 SVDQ_IO_FP16 = 1
 
 # Every symbol include/svdq.h declares.
 EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_prepack_weights",
-            "svdq_w4a4_gemm_prepacked", "svdq_query_plan", "svdq_lora_stage_bytes",
-            "svdq_read_device_status", "svdq_status_string", "svdq_version")
+            "svdq_w4a4_gemm_prepacked", "svdq_w4a4_gemm_split", "svdq_workspace_size",
+            "svdq_query_plan", "svdq_lora_stage_bytes", "svdq_read_device_status",
+            "svdq_status_string", "svdq_version")
 
 
 class SvdqOptions(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("debug_fault", ctypes.c_int32), ("cta_group", ctypes.c_int32),
-                ("io_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("io_dtype", ctypes.c_int32), ("k_splits", ctypes.c_int32)]
 
 
 class SvdqPlan(ctypes.Structure):
@@ -50,7 +52,8 @@ class SvdqPlan(ctypes.Structure):
                 ("tmem_cols", ctypes.c_int32), ("tmem_cols_used", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("num_tiles", ctypes.c_int64),
                 ("grid", ctypes.c_int32), ("sm_count", ctypes.c_int32),
-                ("kblocks_per_stage", ctypes.c_int32)]
+                ("kblocks_per_stage", ctypes.c_int32), ("k_splits", ctypes.c_int32),
+                ("num_units", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -92,6 +95,11 @@ def load(path: Optional[str] = None):
         lib.svdq_w4a4_gemm_prepacked.restype = ctypes.c_int
         lib.svdq_w4a4_gemm_prepacked.argtypes = ([vp] * 9 + [i64] * 4 +
                                                  [ctypes.POINTER(SvdqOptions), vp])
+        lib.svdq_w4a4_gemm_split.restype = ctypes.c_int
+        lib.svdq_w4a4_gemm_split.argtypes = ([vp] * 9 + [i64] * 4 +
+                                             [ctypes.POINTER(SvdqOptions), i32, vp, i64, vp])
+        lib.svdq_workspace_size.restype = i64
+        lib.svdq_workspace_size.argtypes = [i64] * 4 + [ctypes.POINTER(SvdqOptions), i32]
         lib.svdq_query_plan.restype = ctypes.c_int
         lib.svdq_query_plan.argtypes = [i64] * 4 + [ctypes.POINTER(SvdqOptions), i32,
                                                     ctypes.POINTER(SvdqPlan)]
@@ -174,8 +182,29 @@ def svdq_w4a4_gemm_prepacked(act, wgt, ascales, wscales_packed, lora_act_in, lor
                  out, stream, options, check, prepacked=True)
 
 
+def svdq_w4a4_gemm_split(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out,
+                         workspace, stream=None, options=None, weights_prepacked: bool = False,
+                         check: bool = True) -> int:
+    """The operator with split-K for shapes that leave most SMs idle (see
+    include/svdq.h).  ``workspace`` is a zero-filled CUDA uint8 tensor of at
+    least svdq_workspace_size(...) bytes, reused across calls (calls sharing
+    it must not overlap on the GPU).  With ``weights_prepacked`` the weights
+    come from svdq_prepack_weights."""
+    return _gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, stream,
+                 options, check, prepacked=weights_prepacked, workspace=workspace)
+
+
+def svdq_workspace_size(M: int, N: int, K: int, R: int, options=None, sm_count: int = 0) -> int:
+    """Bytes of workspace svdq_w4a4_gemm_split needs (0: the plan does not split)."""
+    opts = _opts(options)
+    n = load().svdq_workspace_size(M, N, K, R, ctypes.byref(opts) if opts else None, sm_count)
+    if n < 0:
+        raise SvdqError(int(n), "svdq_workspace_size")
+    return int(n)
+
+
 def _gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, stream, options,
-          check, prepacked):
+          check, prepacked, workspace=None):
     import torch
 
     M, kh = act.shape
@@ -209,14 +238,22 @@ def _gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, 
     args = [_ptr(act), _ptr(wgt), _ptr(ascales), _ptr(wscales), _ptr(lora_act_in),
             _ptr(lora_up), _ptr(wcscale), _ptr(bias), _ptr(out), M, N, K, R]
     with torch.cuda.device(act.device):
-        if prepacked:
+        if workspace is not None:
+            if workspace.dtype != torch.uint8 or not workspace.is_cuda or \
+                    not workspace.is_contiguous():
+                raise ValueError("workspace: expected a contiguous CUDA uint8 tensor")
+            rc = lib.svdq_w4a4_gemm_split(*args, ctypes.byref(opts) if opts else None,
+                                          1 if prepacked else 0, workspace.data_ptr(),
+                                          workspace.numel(), h)
+        elif prepacked:
             rc = lib.svdq_w4a4_gemm_prepacked(*args, ctypes.byref(opts) if opts else None, h)
         elif opts is None:
             rc = lib.svdq_w4a4_gemm(*args, h)
         else:
             rc = lib.svdq_w4a4_gemm_ex(*args, ctypes.byref(opts), h)
     if check and rc != SVDQ_OK:
-        raise SvdqError(rc, "svdq_w4a4_gemm_prepacked" if prepacked else "svdq_w4a4_gemm")
+        raise SvdqError(rc, "svdq_w4a4_gemm_split" if workspace is not None else
+                        "svdq_w4a4_gemm_prepacked" if prepacked else "svdq_w4a4_gemm")
     return rc
 
 

@@ -7,8 +7,10 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <ctime>
 #include <mutex>
 
 #include "svdq.h"
@@ -25,6 +27,9 @@ namespace {
 constexpr int kGb300SmemOptin = 232448;  // 227 KB dynamic shared memory per block
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultTimeoutMs = 2000;
+constexpr int kMaxSplits = 8;
+constexpr int kMinSplitBlocks = 8;  // planner's minimum K blocks per split
+constexpr int64_t kWsAlign = 256;
 
 struct DeviceInfo {
   bool probed = false;
@@ -32,9 +37,10 @@ struct DeviceInfo {
   int sm_count = 0;
   int smem_optin = 0;
   int* status = nullptr;
-  // per kernel: (1,128), (1,256), (2,256) with bf16 I/O, then the same with fp16
-  bool attr_set[6] = {false, false, false, false, false, false};
-  int max_clusters[6] = {0, 0, 0, 0, 0, 0};
+  // per kernel: (1,128), (1,256), (2,256) with bf16 I/O, the same with fp16,
+  // then those six with split-K
+  bool attr_set[12] = {};
+  int max_clusters[12] = {};
 };
 
 std::mutex g_mutex;
@@ -57,6 +63,9 @@ struct Plan {
   int tmem_cols_used = 0;
   int tiles_m = 0, tiles_n = 0;
   long long num_tiles = 0;
+  int splits = 1;
+  long long num_units = 0;
+  int64_t ws_partial_bytes = 0, ws_flag_bytes = 0;
   int grid = 0;  // CTAs
   int sm_count = 0;
   int group_m = 0;
@@ -71,7 +80,7 @@ int validate_options(const svdq_options_t* o) {
   if (o->cta_group < 0 || o->cta_group > 2) return SVDQ_ERR_BAD_OPTION;
   if (o->cta_group == 2 && o->tile_n == 128) return SVDQ_ERR_BAD_OPTION;
   if (o->io_dtype != SVDQ_IO_BF16 && o->io_dtype != SVDQ_IO_FP16) return SVDQ_ERR_BAD_OPTION;
-  if (o->reserved != 0) return SVDQ_ERR_BAD_OPTION;
+  if (o->k_splits < -1 || o->k_splits > kMaxSplits) return SVDQ_ERR_BAD_OPTION;
   return SVDQ_OK;
 }
 
@@ -152,8 +161,32 @@ void choose_tile(int64_t M, int64_t N, const svdq_options_t* o, int sm_count, in
   *bn = bb;
 }
 
+// K splits (split-K), for launches whose tiles leave more than half of the
+// clusters idle.  Every unit gets a cluster of its own (units <= clusters that
+// fit at once), so all units of a tile run concurrently and the final split's
+// wait for the other splits' partials always ends.  A split costs about as
+// much as ten K blocks of MMA work (partial store, flag, fold), so the planner
+// keeps at least kMinSplitBlocks K blocks per split: long-K shapes only.
+// `allow` is false for entry points without a workspace.
+int choose_splits(const Plan& pl, const svdq_options_t* o, long long avail, bool allow,
+                  int* splits) {
+  const int ks = o ? o->k_splits : 0;
+  *splits = 1;
+  if (ks >= 2) {
+    if (!allow) return SVDQ_ERR_WORKSPACE;
+    if (ks > pl.main_items || pl.num_tiles * ks > avail) return SVDQ_ERR_BAD_OPTION;
+    *splits = ks;
+  } else if (allow && ks != 1 && pl.num_tiles * 2 <= avail) {
+    long long sp = avail / pl.num_tiles;
+    if (sp > pl.main_items / kMinSplitBlocks) sp = pl.main_items / kMinSplitBlocks;
+    if (sp > kMaxSplits) sp = kMaxSplits;
+    if (sp >= 2) *splits = static_cast<int>(sp);
+  }
+  return SVDQ_OK;
+}
+
 int make_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* o, int sm_count,
-              int smem_optin, int max_clusters, Plan* out) {
+              int smem_optin, int max_clusters, Plan* out, bool allow_split) {
   Plan pl;
   choose_tile(M, N, o, sm_count, &pl.cta_group, &pl.tile_n);
   const TileInfo ti = tile_info_for(pl.cta_group, pl.tile_n);
@@ -190,10 +223,20 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* 
   pl.sm_count = sm_count;
   long long clusters = sm_count / pl.cta_group;
   if (max_clusters > 0 && clusters > max_clusters) clusters = max_clusters;
-  if (clusters > pl.num_tiles) clusters = pl.num_tiles;
   if (o && o->max_ctas > 0 && clusters * pl.cta_group > o->max_ctas)
     clusters = o->max_ctas / pl.cta_group > 0 ? o->max_ctas / pl.cta_group : 1;
+  int rc = choose_splits(pl, o, clusters, allow_split, &pl.splits);
+  if (rc != SVDQ_OK) return rc;
+  pl.num_units = pl.num_tiles * pl.splits;
+  if (clusters > pl.num_units) clusters = pl.num_units;
   pl.grid = static_cast<int>(clusters * pl.cta_group);
+  if (pl.splits > 1) {
+    // fp32 partial tiles of the non-final splits (one slot per tile, split,
+    // CTA), then one flag per slot and epilogue warp
+    const int64_t slots = static_cast<int64_t>(pl.num_tiles) * (pl.splits - 1) * pl.cta_group;
+    pl.ws_partial_bytes = slots * kBM * pl.tile_n * 4;
+    pl.ws_flag_bytes = slots * 4 * 4;
+  }
   pl.group_m = pl.tiles_m < 8 ? (pl.tiles_m > 0 ? pl.tiles_m : 1) : 8;
   *out = pl;
   return SVDQ_OK;
@@ -246,18 +289,18 @@ int probe_device(int* dev_out, DeviceInfo** info_out) {
   return SVDQ_OK;
 }
 
-constexpr int kernel_index(int cg, int bn, bool f16) {
-  return (cg == 2 ? 2 : (bn == 256 ? 1 : 0)) + (f16 ? 3 : 0);
+constexpr int kernel_index(int cg, int bn, bool f16, bool sk) {
+  return (cg == 2 ? 2 : (bn == 256 ? 1 : 0)) + (f16 ? 3 : 0) + (sk ? 6 : 0);
 }
 
 // Once per device and kernel: opt in to the shared memory and find how many
 // clusters fit at once.
-template <int CG, int BN, bool F16>
+template <int CG, int BN, bool F16, bool SK>
 int ensure_kernel(DeviceInfo* d, int smem_bytes) {
   std::lock_guard<std::mutex> lock(g_mutex);
-  const int idx = kernel_index(CG, BN, F16);
+  const int idx = kernel_index(CG, BN, F16, SK);
   if (!d->attr_set[idx]) {
-    auto k = svdq_w4a4_kernel<CG, BN, kbi_for<CG>(), F16>;
+    auto k = svdq_w4a4_kernel<CG, BN, kbi_for<CG>(), F16, SK>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_optin) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -311,7 +354,7 @@ struct Operands {
   void* out;
 };
 
-template <int CG, int BN, bool F16>
+template <int CG, int BN, bool F16, bool SK>
 int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams& kp, int64_t M,
            int64_t N, int64_t K, int64_t R, cudaStream_t stream) {
   constexpr int KBI = kbi_for<CG>();
@@ -402,8 +445,9 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CG == 2 ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, svdq_w4a4_kernel<CG, BN, KBI, F16>, tm[0], tm[1], tm[2],
-                                           tm[3], tm[4], tm[5], tm[6], tm[7], kp);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, svdq_w4a4_kernel<CG, BN, KBI, F16, SK>, tm[0], tm[1], tm[2],
+                         tm[3], tm[4], tm[5], tm[6], tm[7], kp);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return SVDQ_ERR_LAUNCH;
@@ -413,12 +457,77 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Runtime (CTA group, tile, I/O type, split-K) -> kernel instance.
+int ensure_any(int cg, int bn, bool f16, bool sk, DeviceInfo* d) {
+  const int so = d->smem_optin;
+  if (sk) {
+    if (cg == 2)
+      return f16 ? ensure_kernel<2, 256, true, true>(d, so)
+                 : ensure_kernel<2, 256, false, true>(d, so);
+    if (bn == 256)
+      return f16 ? ensure_kernel<1, 256, true, true>(d, so)
+                 : ensure_kernel<1, 256, false, true>(d, so);
+    return f16 ? ensure_kernel<1, 128, true, true>(d, so)
+               : ensure_kernel<1, 128, false, true>(d, so);
+  }
+  if (cg == 2)
+    return f16 ? ensure_kernel<2, 256, true, false>(d, so)
+               : ensure_kernel<2, 256, false, false>(d, so);
+  if (bn == 256)
+    return f16 ? ensure_kernel<1, 256, true, false>(d, so)
+               : ensure_kernel<1, 256, false, false>(d, so);
+  return f16 ? ensure_kernel<1, 128, true, false>(d, so)
+             : ensure_kernel<1, 128, false, false>(d, so);
+}
+
+template <bool F16, bool SK>
+int launch_any(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams& kp, int64_t M,
+               int64_t N, int64_t K, int64_t R, cudaStream_t s) {
+  if (pl.cta_group == 2) return launch<2, 256, F16, SK>(pl, dinfo, op, kp, M, N, K, R, s);
+  if (pl.tile_n == 256) return launch<1, 256, F16, SK>(pl, dinfo, op, kp, M, N, K, R, s);
+  return launch<1, 128, F16, SK>(pl, dinfo, op, kp, M, N, K, R, s);
+}
+
+// The plan a launch on this device uses: tile choice, the kernel's
+// attributes and co-resident cluster count, then the solver.
+int device_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* options,
+                DeviceInfo* dinfo, bool f16, bool allow_split, Plan* pl) {
+  int cg = 1, bn = 256;
+  choose_tile(M, N, options, dinfo->sm_count, &cg, &bn);
+  // the unsplit instance's co-resident clusters (the split instance has the
+  // same shared memory and threads)
+  int rc = ensure_any(cg, bn, f16, false, dinfo);
+  if (rc != SVDQ_OK) return rc;
+  const int idx = kernel_index(cg, bn, f16, false);
+  if ((rc = make_plan(M, N, K, R, options, dinfo->sm_count, dinfo->smem_optin,
+                      dinfo->max_clusters[idx], pl, allow_split)) != SVDQ_OK)
+    return rc;
+  return pl->splits > 1 ? ensure_any(cg, bn, f16, true, dinfo) : SVDQ_OK;
+}
+
+// Flag value of a split launch: per-process counter from a time-derived
+// start, never 0 (a zero-filled workspace holds no live flag).
+std::atomic<uint32_t> g_epoch{static_cast<uint32_t>(std::time(nullptr)) * 2654435761u};
+uint32_t next_epoch() {
+  uint32_t e = g_epoch.fetch_add(1) + 1;
+  if (e == 0) e = g_epoch.fetch_add(1) + 1;
+  return e;
+}
+
+int64_t ws_flag_offset(const Plan& pl) {
+  return (pl.ws_partial_bytes + kWsAlign - 1) / kWsAlign * kWsAlign;
+}
+int64_t ws_bytes(const Plan& pl) {
+  return pl.splits > 1 ? ws_flag_offset(pl) + pl.ws_flag_bytes : 0;
+}
+
 // One operator call; `prepacked` selects packed scale words and LU' (from
-// svdq_prepack_weights) for wscales / lora_up.
+// svdq_prepack_weights) for wscales / lora_up; a non-null workspace allows
+// split-K.
 int run_gemm(const void* act, const void* wgt, const void* ascales, const void* wscales,
              const float* lora_act_in, const void* lora_up, const void* wcscale, const void* bias,
              void* out, int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* options,
-             void* stream, bool prepacked) {
+             void* stream, bool prepacked, void* workspace, int64_t workspace_bytes) {
   int rc = validate_options(options);
   if (rc != SVDQ_OK) return rc;
   const bool f16 = options != nullptr && options->io_dtype == SVDQ_IO_FP16;
@@ -434,24 +543,8 @@ int run_gemm(const void* act, const void* wgt, const void* ascales, const void* 
   DeviceInfo* dinfo = nullptr;
   if ((rc = probe_device(&dev, &dinfo)) != SVDQ_OK) return rc;
   Plan pl;
-  {
-    int cg = 1, bn = 256;
-    choose_tile(M, N, options, dinfo->sm_count, &cg, &bn);
-    if (cg == 2)
-      rc = f16 ? ensure_kernel<2, 256, true>(dinfo, dinfo->smem_optin)
-               : ensure_kernel<2, 256, false>(dinfo, dinfo->smem_optin);
-    else if (bn == 256)
-      rc = f16 ? ensure_kernel<1, 256, true>(dinfo, dinfo->smem_optin)
-               : ensure_kernel<1, 256, false>(dinfo, dinfo->smem_optin);
-    else
-      rc = f16 ? ensure_kernel<1, 128, true>(dinfo, dinfo->smem_optin)
-               : ensure_kernel<1, 128, false>(dinfo, dinfo->smem_optin);
-    if (rc != SVDQ_OK) return rc;
-    const int idx = kernel_index(cg, bn, f16);
-    if ((rc = make_plan(M, N, K, R, options, dinfo->sm_count, dinfo->smem_optin,
-                        dinfo->max_clusters[idx], &pl)) != SVDQ_OK)
-      return rc;
-  }
+  if ((rc = device_plan(M, N, K, R, options, dinfo, f16, workspace != nullptr, &pl)) != SVDQ_OK)
+    return rc;
 
   KParams kp;
   std::memset(&kp, 0, sizeof kp);
@@ -470,6 +563,14 @@ int run_gemm(const void* act, const void* wgt, const void* ascales, const void* 
   kp.num_stages = pl.stages;
   kp.lora_tma = (R > 0 && R % 8 == 0);
   kp.prepacked = prepacked ? 1 : 0;
+  kp.splits = pl.splits;
+  kp.num_units = static_cast<int>(pl.num_units);
+  if (pl.splits > 1) {
+    if (!aligned(workspace, kWsAlign) || workspace_bytes < ws_bytes(pl)) return SVDQ_ERR_WORKSPACE;
+    kp.partials = static_cast<float4*>(workspace);
+    kp.flags = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + ws_flag_offset(pl));
+    kp.epoch = next_epoch();
+  }
   kp.debug_fault = options ? options->debug_fault : 0;
   const int tmo = (options && options->timeout_ms) ? options->timeout_ms : kDefaultTimeoutMs;
   kp.timeout_ns = static_cast<unsigned long long>(tmo) * 1000000ull;
@@ -481,14 +582,12 @@ int run_gemm(const void* act, const void* wgt, const void* ascales, const void* 
 
   const Operands op{act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (f16) {
-    if (pl.cta_group == 2) return launch<2, 256, true>(pl, dinfo, op, kp, M, N, K, R, s);
-    if (pl.tile_n == 256) return launch<1, 256, true>(pl, dinfo, op, kp, M, N, K, R, s);
-    return launch<1, 128, true>(pl, dinfo, op, kp, M, N, K, R, s);
-  }
-  if (pl.cta_group == 2) return launch<2, 256, false>(pl, dinfo, op, kp, M, N, K, R, s);
-  if (pl.tile_n == 256) return launch<1, 256, false>(pl, dinfo, op, kp, M, N, K, R, s);
-  return launch<1, 128, false>(pl, dinfo, op, kp, M, N, K, R, s);
+  const bool sk = pl.splits > 1;
+  if (f16)
+    return sk ? launch_any<true, true>(pl, dinfo, op, kp, M, N, K, R, s)
+              : launch_any<true, false>(pl, dinfo, op, kp, M, N, K, R, s);
+  return sk ? launch_any<false, true>(pl, dinfo, op, kp, M, N, K, R, s)
+            : launch_any<false, false>(pl, dinfo, op, kp, M, N, K, R, s);
 }
 
 }  // namespace
@@ -502,7 +601,7 @@ extern "C" int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* a
                                  void* out, int64_t M, int64_t N, int64_t K, int64_t R,
                                  const svdq_options_t* options, void* stream) {
   return run_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, M, N, K,
-                  R, options, stream, false);
+                  R, options, stream, false, nullptr, 0);
 }
 
 extern "C" int svdq_w4a4_gemm_prepacked(const void* act, const void* wgt, const void* ascales,
@@ -512,7 +611,40 @@ extern "C" int svdq_w4a4_gemm_prepacked(const void* act, const void* wgt, const 
                                         int64_t K, int64_t R, const svdq_options_t* options,
                                         void* stream) {
   return run_gemm(act, wgt, ascales, wscales_packed, lora_act_in, lora_up_packed, wcscale, bias,
-                  out, M, N, K, R, options, stream, true);
+                  out, M, N, K, R, options, stream, true, nullptr, 0);
+}
+
+extern "C" int svdq_w4a4_gemm_split(const void* act, const void* wgt, const void* ascales,
+                                    const void* wscales, const float* lora_act_in,
+                                    const void* lora_up, const void* wcscale, const void* bias,
+                                    void* out, int64_t M, int64_t N, int64_t K, int64_t R,
+                                    const svdq_options_t* options, int32_t weights_prepacked,
+                                    void* workspace, int64_t workspace_bytes, void* stream) {
+  if (weights_prepacked != 0 && weights_prepacked != 1) return SVDQ_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < 0) return SVDQ_ERR_WORKSPACE;
+  return run_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, M, N, K,
+                  R, options, stream, weights_prepacked == 1, workspace, workspace_bytes);
+}
+
+extern "C" int64_t svdq_workspace_size(int64_t M, int64_t N, int64_t K, int64_t R,
+                                       const svdq_options_t* options, int32_t sm_count) {
+  int rc = validate_options(options);
+  if (rc != SVDQ_OK) return rc;
+  if ((rc = validate_shape(M, N, K, R)) != SVDQ_OK) return rc;
+  if (M == 0 || N == 0) return 0;
+  Plan pl;
+  if (sm_count <= 0) {
+    // exactly the plan a launch on the current device makes
+    int dev = 0;
+    DeviceInfo* d = nullptr;
+    if ((rc = probe_device(&dev, &d)) != SVDQ_OK) return rc;
+    const bool f16 = options != nullptr && options->io_dtype == SVDQ_IO_FP16;
+    if ((rc = device_plan(M, N, K, R, options, d, f16, true, &pl)) != SVDQ_OK) return rc;
+  } else if ((rc = make_plan(M, N, K, R, options, sm_count, kGb300SmemOptin, 0, &pl, true)) !=
+             SVDQ_OK) {
+    return rc;
+  }
+  return ws_bytes(pl);
 }
 
 extern "C" int svdq_prepack_weights(const void* wscales, const void* lora_up,
@@ -578,7 +710,9 @@ extern "C" int svdq_query_plan(int64_t M, int64_t N, int64_t K, int64_t R,
     smem = d->smem_optin;
   }
   Plan pl;
-  if ((rc = make_plan(M, N, K, R, options, sm_count, smem, 0, &pl)) != SVDQ_OK) return rc;
+  if ((rc = make_plan(M, N, K, R, options, sm_count, smem, 0, &pl,
+                      options != nullptr && options->k_splits != 0)) != SVDQ_OK)
+    return rc;
   std::memset(plan, 0, sizeof *plan);
   plan->tile_m = kBM * pl.cta_group;
   plan->tile_n = pl.tile_n;
@@ -598,6 +732,9 @@ extern "C" int svdq_query_plan(int64_t M, int64_t N, int64_t K, int64_t R,
   plan->grid = pl.grid;
   plan->sm_count = sm_count;
   plan->kblocks_per_stage = pl.kbi;
+  plan->k_splits = pl.splits;
+  plan->num_units = pl.num_units;
+  plan->workspace_bytes = ws_bytes(pl);
   return SVDQ_OK;
 }
 
@@ -648,8 +785,9 @@ extern "C" const char* svdq_status_string(int status) {
     case SVDQ_ERR_CUDA: return "SVDQ_ERR_CUDA";
     case SVDQ_ERR_TIMEOUT: return "SVDQ_ERR_TIMEOUT";
     case SVDQ_ERR_BAD_OPTION: return "SVDQ_ERR_BAD_OPTION";
+    case SVDQ_ERR_WORKSPACE: return "SVDQ_ERR_WORKSPACE";
     default: return "SVDQ_ERR_UNKNOWN";
   }
 }
 
-extern "C" int svdq_version(void) { return 200; }
+extern "C" int svdq_version(void) { return 300; }

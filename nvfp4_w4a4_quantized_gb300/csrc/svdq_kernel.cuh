@@ -96,6 +96,7 @@ enum WaitSite : int {
   kSiteLoraAuxFull = 6,
   kSiteSfAuxFull = 7,
   kSiteEpiAccFull = 8,
+  kSiteSplitFlag = 10,
 };
 
 constexpr int kStatusTimeout = -7;  // == SVDQ_ERR_TIMEOUT
@@ -167,6 +168,11 @@ struct KParams {
   int num_stages;
   int lora_tma;     // R % 8 == 0: LoRA rows arrive by TMA; else direct loads
   int prepacked;    // weights prepacked: scale words [K/64][N], lora_up = LU'
+  int splits;       // K splits per tile (1: every unit is a whole tile)
+  int num_units;    // num_tiles * splits
+  unsigned int epoch;     // split-K: the value this launch's flags are raised to
+  float4* partials;       // split-K: fp32 partial tiles of the non-final splits
+  unsigned int* flags;    // split-K: one per (tile, non-final split, CTA, epilogue warp)
   int debug_fault;
   unsigned long long timeout_ns;
   const float* lora_act_in;
@@ -197,6 +203,40 @@ __device__ __forceinline__ int k_rotation(const KParams& p, int mb, int nb) {
 __device__ __forceinline__ int k_item(const KParams& p, int main_item, int rot) {
   const int it = main_item + rot;
   return it >= p.main_items ? it - p.main_items : it;
+}
+
+// A unit of work: one output tile, or one of its `splits` K ranges.  Split s
+// covers main K blocks [s * main_items / splits, (s+1) * main_items / splits)
+// and split 0 also carries the LoRA items; the last split adds the other
+// splits' partial tiles and writes the output.  Units u = tile * splits + s,
+// so the units of a tile run on consecutive clusters.
+struct Unit {
+  int tile, split, lora, kb_begin, nkb;
+};
+// SK: the kernel instance that splits (the others have splits == 1 built in).
+template <bool SK>
+__device__ __forceinline__ Unit unit_of(const KParams& p, int u) {
+  Unit w;
+  if (!SK) {
+    w.tile = u;
+    w.split = 0;
+    w.kb_begin = 0;
+    w.nkb = p.main_items;
+    w.lora = p.lora_blocks;
+    return w;
+  }
+  w.tile = u / p.splits;
+  w.split = u - w.tile * p.splits;
+  w.kb_begin = (w.split * p.main_items) / p.splits;
+  w.nkb = ((w.split + 1) * p.main_items) / p.splits - w.kb_begin;
+  w.lora = (w.split == 0) ? p.lora_blocks : 0;
+  return w;
+}
+// K item of the unit's main item `mi`: a whole tile keeps the per-tile
+// rotation, a split walks its own range in order.
+template <bool SK>
+__device__ __forceinline__ int unit_k_item(const KParams& p, const Unit& w, int mi, int rot) {
+  return SK ? w.kb_begin + mi : k_item(p, mi, rot);
 }
 
 struct Ctl {
@@ -240,6 +280,22 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, int
                                               const Ctl& c) {
   const bool ok = wait_bar<CLUSTER>(bar, parity, site, c);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Split-K: bounded wait until another split's flag holds this launch's epoch.
+__device__ __forceinline__ bool wait_flag(const unsigned int* f, unsigned int v, const Ctl& c) {
+  if (ptx::ld_acquire_gpu(f) == v) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    __nanosleep(64);
+    if (ptx::ld_acquire_gpu(f) == v) return true;
+    if (*c.abort_flag) return false;
+    if (ptx::globaltimer() - t0 > c.timeout_ns) {
+      *c.abort_flag = 1;
+      report_timeout(c.status, kSiteSplitFlag);
+      return false;
+    }
+  }
 }
 
 // Teardown wait: ignores the abort flag, short fixed limit.
@@ -424,7 +480,7 @@ __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p,
   }
 }
 
-template <int CG, int BN, int KBI, bool F16>
+template <int CG, int BN, int KBI, bool F16, bool SK>
 __global__ void __launch_bounds__(kThreads, 1)
     svdq_w4a4_kernel(const __grid_constant__ CUtensorMap tm_act,
                      const __grid_constant__ CUtensorMap tm_wgt,
@@ -442,7 +498,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = static_cast<int>(threadIdx.x) / 32;
   const int lane = static_cast<int>(threadIdx.x) % 32;
   const int S = p.num_stages;
-  const int n_items = p.lora_blocks + p.main_items;
   const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
   const bool leader = (rank == 0);
   const int cluster_id = static_cast<int>(blockIdx.x) / CG;
@@ -518,7 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool stage_wc = p.wcscale != nullptr && !p.prepacked;
       const uint32_t lora_aux_bytes =
           kBM * kLoraRanks * 4 + L::kBNc * 64 + (stage_wc ? 2 * L::kBNc : 0);
-      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+      for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+        const Unit w = unit_of<SK>(p, u);
+        const int t = w.tile;
+        const int n_items = w.lora + w.nkb;
         int mb, nb;
         tile_coords(p, t, mb, nb);
         const int m0 = mb * kBM * CG, n0 = nb * BN;
@@ -539,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // it tracks by parity, LoRA items (no act / wgt loads) included.
             ptx::mbar_arrive(ab);
           }
-          if (i < p.lora_blocks) {
+          if (i < w.lora) {
             if (role == 0) {
               if (p.lora_tma) {
                 ptx::mbar_arrive_expect_tx(ab, lora_aux_bytes);
@@ -555,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (leader) ptx::mbar_arrive(full(stage));
             }
           } else {
-            const int kb0 = KBI * k_item(p, i - p.lora_blocks, rot);
+            const int kb0 = KBI * unit_k_item<SK>(p, w, i - w.lora, rot);
             const int nkb = min(KBI, p.k_blocks - kb0);
             if (role == 0) {
               ptx::mbar_arrive_expect_tx(ab, main_aux_bytes);
@@ -632,7 +690,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t desc_a0 = ptx::desc_kmajor_sw128(sbase + L::kOffA);
       const uint64_t desc_b0 = ptx::desc_kmajor_sw128(sbase + L::kOffB);
       const bool k_ragged = (p.K % kBK) != 0;  // the last K block is partial
-      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++tile_iter) {
+      for (int u = cluster_id; ok && u < p.num_units; u += num_clusters, ++tile_iter) {
+        const Unit w = unit_of<SK>(p, u);
+        const int t = w.tile;
+        const int n_items = w.lora + w.nkb;
         int mb, nb;
         tile_coords(p, t, mb, nb);
         const int rot = k_rotation(p, mb, nb);
@@ -658,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((j & 1u) == me) {
             ptx::tc_fence_after();
             const uint32_t st = sbase + stage * L::kStageBytes;
-            if (i < p.lora_blocks) {
+            if (i < w.lora) {
               const int nsteps = min(2, (p.r16 - kLoraRanks * i) / 16);
               for (int s = 0; s < nsteps; ++s) {
                 const uint64_t ad = ptx::desc_kmajor_sw64(st + L::kLoraLA + 32 * s);
@@ -689,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // K=64 steps present in this item (the last K block may be partial)
               int nsteps = L::kSteps;
               if (k_ragged) {
-                const int kb0 = KBI * k_item(p, i - p.lora_blocks, rot);
+                const int kb0 = KBI * unit_k_item<SK>(p, w, i - w.lora, rot);
                 nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
               }
               if (nsteps == L::kSteps) {
@@ -735,7 +796,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     const uint32_t full_bar0 = to_leader(full(0));
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+    for (int u = cluster_id; u < p.num_units; u += num_clusters) {
+      const Unit w = unit_of<SK>(p, u);
+      const int t = w.tile;
+      const int n_items = w.lora + w.nkb;
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int n_cta = nb * BN + L::kBNc * static_cast<int>(rank);
@@ -745,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (i < p.lora_blocks) {
+        if (i < w.lora) {
           // LU' rows [h kBNc/2, (h+1) kBNc/2) (the scale feeders build LA')
           uint8_t* st = smem + stage * L::kStageBytes;
           const int r0 = (warp - 2) * (L::kBNc / 2);
@@ -792,7 +856,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0)
       for (int a = 0; a < L::kAccStages; ++a) ptx::mbar_arrive_remote(acc_empty0 + 8u * a);
     int tile_iter = 0;
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++tile_iter) {
+    for (int u = cluster_id; u < p.num_units; u += num_clusters, ++tile_iter) {
+      const Unit w = unit_of<SK>(p, u);
+      const int t = w.tile;
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
@@ -823,15 +889,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t acc_phase = static_cast<uint32_t>(tile_iter / L::kAccStages) & 1u;
       if (!warp_wait_bar<false>(acc_full(acc_stage), acc_phase, kSiteEpiAccFull, ctl)) break;
       ptx::tc_fence_after();
+      // Split-K: a non-final split stores its fp32 partial tile (no affine)
+      // and raises its flag; the final split waits for the other splits'
+      // flags and adds their partials before the affine.  Partial slot
+      // (tile, split, CTA) holds this warp's rows as float4 [group][k][lane]
+      // (coalesced: lane-consecutive 16-byte pieces).
+      const bool write_partial = SK && w.split < p.splits - 1;
+      const bool add_partials = SK && !write_partial;
+      // slot of (tile, split sp, CTA) = (t (splits - 1) + sp) CG + rank
+      const size_t slot0 = static_cast<size_t>(t) * static_cast<size_t>(p.splits - 1) * CG + rank;
+      constexpr size_t kSlotF4 = static_cast<size_t>(kBM) * BN / 4;  // float4 per slot
+      const float4* part0 = p.partials + slot0 * kSlotF4 + (q * (BN / 32) * 8) * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc_stage * BN);
+      constexpr int kGroups = BN / 32;
+      auto gcol = [&](int g) { return taddr + 128 * (g >> 2) + 8 * (g & 3); };
+      if (write_partial) {
+        for (int g = 0; g < kGroups; ++g) {
+          uint32_t v[4][8];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(g) + 32 * b, v[b]);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int b = 0; b < 4; ++b) ptx::tmem_st_32x32b_x8(gcol(g) + 32 * b, zero8);
+          float4* dst = const_cast<float4*>(part0) + static_cast<size_t>(w.split) * CG * kSlotF4 +
+                        g * 256;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            __stcg(dst + 32 * k, make_float4(__uint_as_float(v[0][k]), __uint_as_float(v[1][k]),
+                                             __uint_as_float(v[2][k]), __uint_as_float(v[3][k])));
+        }
+        // read and cleared: release the accumulator, then publish the partial
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
+        __threadfence();  // every lane's partial stores are visible device-wide ...
+        __syncwarp();     // ... before lane 0 raises the flag
+        if (lane == 0)
+          ptx::st_release_gpu(p.flags + (slot0 + static_cast<size_t>(w.split) * CG) * 4 + q,
+                              p.epoch);
+        continue;
+      }
+      if (add_partials) {
+        bool got = true;
+        for (int sp = 0; sp < p.splits - 1 && got; ++sp)
+          got = wait_flag(p.flags + (slot0 + static_cast<size_t>(sp) * CG) * 4 + q, p.epoch, ctl);
+        if (!__all_sync(0xffffffffu, got)) break;
+        // fold the other splits' partials into this accumulator (fp32)
+        for (int g = 0; g < kGroups; ++g) {
+          uint32_t v[4][8];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(g) + 32 * b, v[b]);
+          ptx::tmem_wait_ld();
+          for (int sp = 0; sp < p.splits - 1; ++sp) {
+            const float4* src = part0 + static_cast<size_t>(sp) * CG * kSlotF4 + g * 256;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float4 a = __ldcg(src + 32 * k);
+              v[0][k] = __float_as_uint(__uint_as_float(v[0][k]) + a.x);
+              v[1][k] = __float_as_uint(__uint_as_float(v[1][k]) + a.y);
+              v[2][k] = __float_as_uint(__uint_as_float(v[2][k]) + a.z);
+              v[3][k] = __float_as_uint(__uint_as_float(v[3][k]) + a.w);
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < 4; ++b) ptx::tmem_st_32x32b_x8(gcol(g) + 32 * b, v[b]);
+        }
+        ptx::tmem_wait_st();
+      }
       // Column group g (32 output columns n0 + 32g + 4k + b, k < 8, b < 4) sits in
       // accumulator columns 128h + 32b + 8(g % 4) + k, h = g / 4.  Groups are
       // software-pipelined: group g+1's tensor-memory loads are in flight while
       // group g is scaled, converted and staged; two groups make one 64-column
       // TMA store.
-      constexpr int kGroups = BN / 32;
-      auto gcol = [&](int g) { return taddr + 128 * (g >> 2) + 8 * (g & 3); };
       uint32_t ra[4][8], rb[4][8];
 #pragma unroll
       for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(0) + 32 * b, ra[b]);
@@ -856,12 +987,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int o = 32 * g + 4 * k;
-          const float4 w = *reinterpret_cast<const float4*>(wb + o);
+          const float4 wc4 = *reinterpret_cast<const float4*>(wb + o);
           const float4 bb = *reinterpret_cast<const float4*>(wb + BN + o);
-          const float y0 = fmaf(__uint_as_float(cur[0][k]), w.x, bb.x);
-          const float y1 = fmaf(__uint_as_float(cur[1][k]), w.y, bb.y);
-          const float y2 = fmaf(__uint_as_float(cur[2][k]), w.z, bb.z);
-          const float y3 = fmaf(__uint_as_float(cur[3][k]), w.w, bb.w);
+          const float y0 = fmaf(__uint_as_float(cur[0][k]), wc4.x, bb.x);
+          const float y1 = fmaf(__uint_as_float(cur[1][k]), wc4.y, bb.y);
+          const float y2 = fmaf(__uint_as_float(cur[2][k]), wc4.z, bb.z);
+          const float y3 = fmaf(__uint_as_float(cur[3][k]), wc4.w, bb.w);
           pk[2 * k] = H::pack(y0, y1);
           pk[2 * k + 1] = H::pack(y2, y3);
         }
@@ -899,7 +1030,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     const uint32_t full_bar0 = to_leader(full(0));
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+    for (int u = cluster_id; u < p.num_units; u += num_clusters) {
+      const Unit w = unit_of<SK>(p, u);
+      const int t = w.tile;
+      const int n_items = w.lora + w.nkb;
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
@@ -909,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (i < p.lora_blocks) {
+        if (i < w.lora) {
           // LoRA item: this warp builds LA' rows [32q, 32q + 32)
           uint8_t* st = smem + stage * L::kStageBytes;
           if (p.lora_tma)

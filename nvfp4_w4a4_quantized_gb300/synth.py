@@ -50,6 +50,8 @@ TINY = Workload("tiny_256x256x256_r32", 256, 256, 256, 32, 0)
 ATTN_PROJ = Workload("attn_proj_4096x3072x3072_r32", 4096, 3072, 3072, 32, 1)
 MLP_UP = Workload("mlp_up_4096x12288x3072_r32", 4096, 12288, 3072, 32, 2)
 MLP_DOWN = Workload("mlp_down_4096x3072x12288_r128", 4096, 3072, 12288, 128, 3)
+# The MLP-down projection at 256 tokens: few tiles, long K (the split-K case).
+MLP_DOWN_SMALL_M = Workload("mlp_down_256x3072x12288_r128", 256, 3072, 12288, 128, 5)
 
 
 def sweep_workloads() -> List[Workload]:
@@ -64,7 +66,7 @@ def sweep_workloads() -> List[Workload]:
 
 
 WORKLOADS: Dict[str, Workload] = {
-    w.name: w for w in [TINY, ATTN_PROJ, MLP_UP, MLP_DOWN] + sweep_workloads()
+    w.name: w for w in [TINY, ATTN_PROJ, MLP_UP, MLP_DOWN, MLP_DOWN_SMALL_M] + sweep_workloads()
 }
 
 

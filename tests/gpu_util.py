@@ -95,3 +95,29 @@ def run_gpu_prepacked(inp, M, N, K, R, options=None):
     code, site, block = binding.svdq_read_device_status(clear=True)
     assert code == 0, f"device status {code} at wait site {site}, CTA {block}"
     return out.to(torch.float64).cpu().numpy()
+
+
+def run_gpu_split(inp, M, N, K, R, options=None, prepacked=False, workspace=None):
+    """The split-K entry point (svdq_w4a4_gemm_split) on `inp` (CPU tensors);
+    allocates a zero-filled workspace of the planned size unless one is given.
+    Returns (y as float64 numpy, workspace)."""
+    d = prepack_gpu(inp, R) if prepacked else to_device(inp)
+    half = any(isinstance(inp.get(k), torch.Tensor) and inp[k].dtype == torch.float16
+               for k in ("lora_up", "wcscale", "bias"))
+    opts = dict(options or {})
+    if half:
+        opts["io_dtype"] = binding.SVDQ_IO_FP16
+    if workspace is None:
+        nbytes = binding.svdq_workspace_size(M, N, K, R, options=opts)
+        workspace = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+    out = torch.full((M, N), float("nan"), dtype=torch.float16 if half else torch.bfloat16,
+                     device="cuda")
+    binding.svdq_w4a4_gemm_split(d["act"], d["wgt"], d["ascales"], d["wscales"],
+                                 d["lora_act_in"] if R > 0 else None,
+                                 d["lora_up"] if R > 0 else None, d.get("wcscale"),
+                                 d.get("bias"), out, workspace, options=opts,
+                                 weights_prepacked=prepacked)
+    torch.cuda.synchronize()
+    code, site, block = binding.svdq_read_device_status(clear=True)
+    assert code == 0, f"device status {code} at wait site {site}, CTA {block}"
+    return out.to(torch.float64).cpu().numpy(), workspace

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         s = binding.status_string(code)
         assert s.startswith("SVDQ_")
     assert binding.status_string(-99) == "SVDQ_ERR_UNKNOWN"
@@ -90,7 +90,8 @@ def call(lib, M=256, N=256, K=256, R=32, ptrs=None, opts=None, prepacked=False):
     (dict(opts=dict(stages=1)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(stages=9)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(debug_fault=2)), binding.SVDQ_ERR_BAD_OPTION),
-    (dict(opts=dict(reserved=1)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(k_splits=9)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(k_splits=-2)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(io_dtype=2)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(cta_group=3)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(cta_group=2, tile_n=128)), binding.SVDQ_ERR_BAD_OPTION),
@@ -223,3 +224,43 @@ def test_lora_stage_bytes_match_the_pages_probe(lib):
     assert binding.svdq_lora_stage_bytes(128, 256, 32, 2, 1)[1:] == (8192, 16384)
     with pytest.raises(binding.SvdqError):
         binding.svdq_lora_stage_bytes(255, 128, 128, 2, 2)
+
+
+# ---------------------------------------------------------------- split-K planning
+def test_split_plan_small_m_long_k(lib):
+    # 256 x 3072 x 12288: 48 single-CTA 128x128 tiles fill under a third of
+    # 152 SMs and 48 K blocks leave 16 per split
+    plan = binding.svdq_query_plan(256, 3072, 12288, 128, options=dict(k_splits=-1),
+                                   sm_count=SMS)
+    assert (plan["cta_group"], plan["tile_n"]) == (1, 128)
+    assert plan["k_splits"] == 3 and plan["num_units"] == 144 and plan["grid"] == 144
+    slots = 48 * 2 * 1
+    partial = slots * 128 * 128 * 4
+    assert plan["workspace_bytes"] == partial + slots * 16
+    assert binding.svdq_workspace_size(256, 3072, 12288, 128, sm_count=SMS) == \
+        plan["workspace_bytes"]
+    # the default plan (entry points without a workspace) never splits
+    plain = binding.svdq_query_plan(256, 3072, 12288, 128, sm_count=SMS)
+    assert plain["k_splits"] == 1 and plain["workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 3072, 3072), (1024, 12288, 3072), (256, 256, 256),
+                                   (256, 3072, 3072)])
+def test_split_plan_declines(lib, M, N, K):
+    # enough tiles for half the clusters, or fewer than 2 x 8 K blocks: no split
+    plan = binding.svdq_query_plan(M, N, K, 32, options=dict(k_splits=-1), sm_count=SMS)
+    assert plan["k_splits"] == 1 and plan["workspace_bytes"] == 0
+    assert binding.svdq_workspace_size(M, N, K, 32, sm_count=SMS) == 0
+
+
+def test_split_plan_forced_and_rejected(lib):
+    plan = binding.svdq_query_plan(256, 384, 1024, 16, options=dict(k_splits=2, cta_group=1,
+                                                                   tile_n=128), sm_count=SMS)
+    assert plan["k_splits"] == 2 and plan["num_units"] == 2 * plan["num_tiles"]
+    # more splits than K blocks, or more units than clusters: rejected
+    with pytest.raises(binding.SvdqError) as e:
+        binding.svdq_query_plan(256, 384, 512, 16, options=dict(k_splits=3), sm_count=SMS)
+    assert e.value.status == binding.SVDQ_ERR_BAD_OPTION
+    with pytest.raises(binding.SvdqError) as e:
+        binding.svdq_query_plan(4096, 3072, 3072, 32, options=dict(k_splits=2), sm_count=SMS)
+    assert e.value.status == binding.SVDQ_ERR_BAD_OPTION
