@@ -38,6 +38,11 @@ extern "C" {
 #define SVDQ_ERR_BAD_OPTION -8         /* an svdq_options_t field is out of range       */
 #define SVDQ_ERR_WORKSPACE -9          /* split-K needs a workspace: missing, smaller than
                                           svdq_workspace_size, or not 256-byte aligned  */
+#define SVDQ_ERR_SCRATCH_LIMIT -10     /* the plan needs more scratch than the library's
+                                          fixed SVDQ_NOALLOC_SCRATCH_BYTES              */
+
+/* Size of the library's own scratch array (svdq_w4a4_gemm_split_noalloc). */
+#define SVDQ_NOALLOC_SCRATCH_BYTES (16LL << 20)
 
 /* Size limits: M, N <= 2^24 and K <= 2^20 (elements). */
 #define SVDQ_MAX_MN (1LL << 24)
@@ -197,6 +202,33 @@ int svdq_w4a4_gemm_split(const void* act, const void* wgt, const void* ascales,
                          int64_t K, int64_t R, const svdq_options_t* options,
                          int32_t weights_prepacked, void* workspace, int64_t workspace_bytes,
                          void* stream);
+
+/*
+ * svdq_w4a4_gemm_split_noalloc -- svdq_w4a4_gemm_split for callers that cannot
+ * allocate device memory: code that runs while a serving engine has reserved
+ * the whole device for its own memory pool, or inside a runtime that forbids
+ * cudaMalloc after start-up, and so has no workspace to pass.  (The paper has
+ * no counterpart; it is this library's own.)  The split-K partial tiles and
+ * flags live in a scratch array built into the library,
+ * SVDQ_NOALLOC_SCRATCH_BYTES (16 MiB) per GPU that loads it, held until the
+ * process exits; nothing is allocated per call, by this function or by
+ * anything it calls.
+ *
+ * Arguments are those of svdq_w4a4_gemm_split without the workspace.  Plans
+ * needing more than SVDQ_NOALLOC_SCRATCH_BYTES (svdq_workspace_size) return
+ * SVDQ_ERR_SCRATCH_LIMIT before anything is launched.  The first call on a
+ * device looks up the array's device address (a one-time set-up per device);
+ * make that first call before any stream capture.  Every call on a device
+ * shares the one array: calls that overlap on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller.  Flags carry a
+ * per-call value, so nothing needs clearing between calls.
+ */
+int svdq_w4a4_gemm_split_noalloc(const void* act, const void* wgt, const void* ascales,
+                                 const void* wscales, const float* lora_act_in,
+                                 const void* lora_up, const void* wcscale, const void* bias,
+                                 void* out, int64_t M, int64_t N, int64_t K, int64_t R,
+                                 const svdq_options_t* options, int32_t weights_prepacked,
+                                 void* stream);
 
 /* Workspace bytes svdq_w4a4_gemm_split needs for this shape and options
  * (0 when the plan does not split), or a negative status.  sm_count <= 0

@@ -25,13 +25,16 @@ SVDQ_ERR_CUDA = -6
 SVDQ_ERR_TIMEOUT = -7
 SVDQ_ERR_BAD_OPTION = -8
 SVDQ_ERR_WORKSPACE = -9
+SVDQ_ERR_SCRATCH_LIMIT = -10
+SVDQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 SVDQ_IO_BF16 = 0
 SVDQ_IO_FP16 = 1
 
 # Every symbol include/svdq.h declares.
 EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_prepack_weights",
-            "svdq_w4a4_gemm_prepacked", "svdq_w4a4_gemm_split", "svdq_workspace_size",
+            "svdq_w4a4_gemm_prepacked", "svdq_w4a4_gemm_split", "svdq_w4a4_gemm_split_noalloc",
+            "svdq_workspace_size",
             "svdq_query_plan", "svdq_lora_stage_bytes", "svdq_read_device_status",
             "svdq_status_string", "svdq_version")
 
@@ -98,6 +101,9 @@ def load(path: Optional[str] = None):
         lib.svdq_w4a4_gemm_split.restype = ctypes.c_int
         lib.svdq_w4a4_gemm_split.argtypes = ([vp] * 9 + [i64] * 4 +
                                              [ctypes.POINTER(SvdqOptions), i32, vp, i64, vp])
+        lib.svdq_w4a4_gemm_split_noalloc.restype = ctypes.c_int
+        lib.svdq_w4a4_gemm_split_noalloc.argtypes = ([vp] * 9 + [i64] * 4 +
+                                                     [ctypes.POINTER(SvdqOptions), i32, vp])
         lib.svdq_workspace_size.restype = i64
         lib.svdq_workspace_size.argtypes = [i64] * 4 + [ctypes.POINTER(SvdqOptions), i32]
         lib.svdq_query_plan.restype = ctypes.c_int

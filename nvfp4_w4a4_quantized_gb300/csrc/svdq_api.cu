@@ -22,6 +22,11 @@ namespace svdq {
 // Device status word: [0] code, [1] wait site, [2] CTA, [3] spare.
 __device__ int g_device_status[4];
 
+// Scratch of svdq_w4a4_gemm_split_noalloc, for callers that cannot allocate
+// device memory.  Every GPU that loads this library holds it (zero-filled at
+// load) until the process exits; only that entry point touches it.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SVDQ_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int kGb300SmemOptin = 232448;  // 227 KB dynamic shared memory per block
@@ -37,6 +42,7 @@ struct DeviceInfo {
   int sm_count = 0;
   int smem_optin = 0;
   int* status = nullptr;
+  void* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch, looked up once
   // per kernel: (1,128), (1,256), (2,256) with bf16 I/O, the same with fp16,
   // then those six with split-K
   bool attr_set[12] = {};
@@ -786,8 +792,42 @@ extern "C" const char* svdq_status_string(int status) {
     case SVDQ_ERR_TIMEOUT: return "SVDQ_ERR_TIMEOUT";
     case SVDQ_ERR_BAD_OPTION: return "SVDQ_ERR_BAD_OPTION";
     case SVDQ_ERR_WORKSPACE: return "SVDQ_ERR_WORKSPACE";
+    case SVDQ_ERR_SCRATCH_LIMIT: return "SVDQ_ERR_SCRATCH_LIMIT";
     default: return "SVDQ_ERR_UNKNOWN";
   }
 }
 
 extern "C" int svdq_version(void) { return 300; }
+
+extern "C" int svdq_w4a4_gemm_split_noalloc(const void* act, const void* wgt, const void* ascales,
+                                            const void* wscales, const float* lora_act_in,
+                                            const void* lora_up, const void* wcscale,
+                                            const void* bias, void* out, int64_t M, int64_t N,
+                                            int64_t K, int64_t R, const svdq_options_t* options,
+                                            int32_t weights_prepacked, void* stream) {
+  if (weights_prepacked != 0 && weights_prepacked != 1) return SVDQ_ERR_INVALID_ARG;
+  // the plan's scratch need, computed exactly as the launch will plan
+  const int64_t need = svdq_workspace_size(M, N, K, R, options, 0);
+  if (need < 0) return static_cast<int>(need);
+  if (need > SVDQ_NOALLOC_SCRATCH_BYTES) return SVDQ_ERR_SCRATCH_LIMIT;
+  int dev = 0;
+  DeviceInfo* d = nullptr;
+  int rc = probe_device(&dev, &d);
+  if (rc != SVDQ_OK) return rc;
+  {
+    // once per device, with that device current: the array's device address
+    // (in host code the symbol is only a host-side stand-in)
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (d->noalloc_scratch == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return SVDQ_ERR_CUDA;
+      }
+      d->noalloc_scratch = ptr;
+    }
+  }
+  return run_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, M, N, K,
+                  R, options, stream, weights_prepacked == 1, d->noalloc_scratch,
+                  SVDQ_NOALLOC_SCRATCH_BYTES);
+}
