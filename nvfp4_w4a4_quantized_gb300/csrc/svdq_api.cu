@@ -238,10 +238,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* 
   pl.grid = static_cast<int>(clusters * pl.cta_group);
   if (pl.splits > 1) {
     // fp32 partial tiles of the non-final splits (one slot per tile, split,
-    // CTA), then one flag per slot and epilogue warp
+    // CTA), then one flag per slot and epilogue warp (eight per CTA)
     const int64_t slots = static_cast<int64_t>(pl.num_tiles) * (pl.splits - 1) * pl.cta_group;
     pl.ws_partial_bytes = slots * kBM * pl.tile_n * 4;
-    pl.ws_flag_bytes = slots * 4 * 4;
+    pl.ws_flag_bytes = slots * 8 * 4;
   }
   pl.group_m = pl.tiles_m < 8 ? (pl.tiles_m > 0 ? pl.tiles_m : 1) : 8;
   *out = pl;
@@ -407,12 +407,12 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
                        CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
         return rc;
     }
-    // output: one store writes rows 4a + q (a < 32) of a 128-row block
+    // output: one store writes 32 columns of rows 4a + q (a < 32) of a 128-row block
     const uint64_t d_out[3] = {static_cast<uint64_t>(N), M4, 4},
                    s_out[2] = {static_cast<uint64_t>(N) * 8, static_cast<uint64_t>(N) * 2};
-    const uint32_t b_out[3] = {64, 32, 1};
+    const uint32_t b_out[3] = {32, 32, 1};
     if ((rc = encode(&tm[7], kIoType, 3, op.out, d_out, s_out, b_out,
-                     CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
+                     CU_TENSOR_MAP_SWIZZLE_64B)) != SVDQ_OK)
       return rc;
   }
   if (kp.lora_tma) {

@@ -26,7 +26,7 @@
 // row order (warp q's lane a is output row 4a + q) and its columns the B order
 // (column 128h + a + 32b is output column 128h + 4a + b).
 //
-// 15 warps per CTA (480 threads):
+// 19 warps per CTA (608 threads):
 //   warps 0, 12, 13  TMA producers, one thread each, every ring item split
 //                three ways (one issuing thread streams far fewer bytes per
 //                second than three): warp 0 the [16 groups x rows] scale
@@ -41,18 +41,20 @@
 //   warps 2, 3   LoRA operand builders: LU' = round16(LU / wc), half the rows
 //                each, in place in the stage's K-major 64-byte-swizzle layout
 //                (nothing to do for prepacked weights, whose LU' arrives ready).
-//   warps 4..7   epilogue: tcgen05.ld (32 columns at a time, software-
-//                pipelined) -> fma(acc, wc, bias) -> 16-bit -> shared staging
-//                (128-byte swizzle) -> TMA tile store; every column read is
-//                cleared for the next tile and the accumulator released after
-//                the last one.
+//   warps 4..7, 15..18  epilogue, two warps per 32-lane quadrant, each taking
+//                half of the tile's 32-column groups: tcgen05.ld -> fma(acc,
+//                wc, bias) -> 16-bit -> shared staging (64-byte swizzle) -> one
+//                TMA tile store per group; every column read is cleared for the
+//                next tile and each warp releases the accumulator after its
+//                last group (the MMA waits for all eight).
 //   warps 8..11  scale feeders: turn the stage's scale boxes into row-per-lane
 //                words in registers (a 4x4 byte transpose of raw scales, or
 //                plain 16-byte loads of prepacked weight-scale words) and write
 //                them into tensor memory with tcgen05.st (one warp per 32-lane
 //                quadrant), off the MMA pipe; on LoRA items they build
 //                LA' = round16(LA), 32 rows each.
-// Warp 4+q / 8+q own tensor-memory lanes 32q .. 32q+31.
+// Warp w accesses tensor-memory lanes 32(w%4) .. 32(w%4)+31, so epilogue warps
+// 4..7 and 15..18 and scale feeders 8..11 each cover all four quadrants.
 //
 // Per output tile the ring carries ceil(R/32) LoRA items, then ceil(K/256)
 // main items; every role walks the same item sequence, so stage index and
@@ -78,7 +80,7 @@
 
 namespace svdq {
 
-constexpr int kThreads = 480;
+constexpr int kThreads = 608;
 constexpr int kBM = 128;     // output rows per CTA (per-CTA MMA M)
 constexpr int kBK = 256;     // K elements per K block (128 packed bytes per row)
 constexpr int kLoraRanks = 32;  // ranks per LoRA ring item
@@ -137,9 +139,9 @@ struct Layout {
   static constexpr int kSfCols = kSteps * (4 + 4 * kSfbHalves);
   // epilogue, per warp: one 32 x 64 bf16 staging tile (128-byte rows, 128-byte
   // swizzle) and the tile's fp32 wcscale[BN], bias[BN]
-  static constexpr int kEpiStageBytes = 32 * 128;
-  static constexpr int kEpiBytes = 4 * kEpiStageBytes;
-  static constexpr int kWcbBytes = 4 * 2 * BN * 4;
+  static constexpr int kEpiStageBytes = 32 * 64;
+  static constexpr int kEpiBytes = 8 * kEpiStageBytes;
+  static constexpr int kWcbBytes = 8 * BN * 4;
   static constexpr int kBarCount = 5 * kMaxStages + 7;
   static constexpr int kBarBytes = 8 * kBarCount + 16;
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
@@ -531,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(acc_full(a), 2);          // one commit per MMA issuer
-      ptx::mbar_init(acc_empty(a), 4 * CG);    // the epilogue warps of the group
+      ptx::mbar_init(acc_empty(a), 8 * CG);    // the epilogue warps of the group
     }
     ptx::mbar_init(never, 1);
     ptx::mbar_init(drain(0), 1);
@@ -834,22 +836,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
     }
-  } else if (warp < 8) {
+  } else if (warp < 8 || warp >= 15) {
     // ------------------------------------------------------------ epilogue
+    // Two warps per tensor-memory lane quadrant: warps 4..7 take the tile's
+    // first half of the column groups, warps 15..18 the second half.
     const int q = warp & 3;  // tensor-memory lane quadrant of this warp
+    const int eh = warp >= 15 ? 1 : 0;
+    const int ew = 4 * eh + q;  // epilogue warp index
+    constexpr int kGroups = BN / 32;
+    constexpr int kHalfG = kGroups / 2;
+    const int g0 = eh * kHalfG;  // this warp's first column group
     using H = H16<F16>;
     const uint16_t* wcg = p.wcscale;
     const uint16_t* big = p.bias;
-    uint8_t* stg = smem + L::epi_offset(S) + q * L::kEpiStageBytes;
-    float* wb = reinterpret_cast<float*>(smem + L::wcb_offset(S) + q * (8 * BN));  // wc, bias
+    uint8_t* stg = smem + L::epi_offset(S) + ew * L::kEpiStageBytes;
+    // this warp's half of the tile's wcscale, bias as fp32: wb[c], wb[BN/2 + c]
+    float* wb = reinterpret_cast<float*>(smem + L::wcb_offset(S) + ew * (4 * BN));
     const uint32_t acc_empty0 = to_leader(acc_empty(0));
     const uint32_t zero8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     const uint32_t lane_q = static_cast<uint32_t>(32 * q) << 16;
     // The MMAs only accumulate: clear every accumulator buffer once before the
-    // first tile (each warp its own 32 lanes), then hand them to the MMA issuers.
+    // first tile (each warp its own lanes and column groups), then hand them
+    // to the MMA issuers.
     for (int a = 0; a < L::kAccStages; ++a)
-      for (int c = 0; c < BN; c += 8)
-        ptx::tmem_st_32x32b_x8(tmem_base + lane_q + static_cast<uint32_t>(a * BN + c), zero8);
+      for (int g = g0; g < g0 + kHalfG; ++g)
+        for (int b = 0; b < 4; ++b)
+          ptx::tmem_st_32x32b_x8(tmem_base + lane_q +
+                                     static_cast<uint32_t>(a * BN + 128 * (g >> 2) + 8 * (g & 3) +
+                                                           32 * b),
+                                 zero8);
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
     __syncwarp();
@@ -863,15 +878,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(p, t, mb, nb);
       const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
       const int n0 = nb * BN;
-      // This tile's wcscale / bias as fp32 in this warp's own buffer (no other
-      // warp reads it; the previous tile's reads are behind us in program order).
-      if (lane < BN / 8) {
+      // This tile's wcscale / bias (this warp's half) as fp32 in this warp's
+      // own buffer (no other warp reads it; the previous tile's reads are
+      // behind us in program order).
+      if (lane < BN / 16) {
         const int c = 8 * lane;
+        const int n = n0 + 32 * g0 + c;
         uint4 wv = make_uint4(H::kOnes, H::kOnes, H::kOnes, H::kOnes);  // 1.0
         uint4 bv = make_uint4(0u, 0u, 0u, 0u);
-        if (n0 + c < p.N) {
-          if (wcg) wv = __ldg(reinterpret_cast<const uint4*>(wcg + n0 + c));
-          if (big) bv = __ldg(reinterpret_cast<const uint4*>(big + n0 + c));
+        if (n < p.N) {
+          if (wcg) wv = __ldg(reinterpret_cast<const uint4*>(wcg + n));
+          if (big) bv = __ldg(reinterpret_cast<const uint4*>(big + n));
         }
         const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
@@ -879,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4*>(wb + c + 4 * i) =
               make_float4(H::lo(w4[2 * i]), H::hi(w4[2 * i]), H::lo(w4[2 * i + 1]),
                           H::hi(w4[2 * i + 1]));
-          *reinterpret_cast<float4*>(wb + BN + c + 4 * i) =
+          *reinterpret_cast<float4*>(wb + BN / 2 + c + 4 * i) =
               make_float4(H::lo(b4[2 * i]), H::hi(b4[2 * i]), H::lo(b4[2 * i + 1]),
                           H::hi(b4[2 * i + 1]));
         }
@@ -899,13 +916,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // slot of (tile, split sp, CTA) = (t (splits - 1) + sp) CG + rank
       const size_t slot0 = static_cast<size_t>(t) * static_cast<size_t>(p.splits - 1) * CG + rank;
       constexpr size_t kSlotF4 = static_cast<size_t>(kBM) * BN / 4;  // float4 per slot
-      const float4* part0 = p.partials + slot0 * kSlotF4 + (q * (BN / 32) * 8) * 32 + lane;
+      const float4* part0 = p.partials + slot0 * kSlotF4 + (q * kGroups * 8) * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc_stage * BN);
-      constexpr int kGroups = BN / 32;
       auto gcol = [&](int g) { return taddr + 128 * (g >> 2) + 8 * (g & 3); };
+      // one flag per (slot, epilogue warp)
+      auto flag = [&](int sp) { return p.flags + (slot0 + static_cast<size_t>(sp) * CG) * 8 + ew; };
       if (write_partial) {
-        for (int g = 0; g < kGroups; ++g) {
+        for (int g = g0; g < g0 + kHalfG; ++g) {
           uint32_t v[4][8];
 #pragma unroll
           for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(g) + 32 * b, v[b]);
@@ -926,18 +944,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
         __threadfence();  // every lane's partial stores are visible device-wide ...
         __syncwarp();     // ... before lane 0 raises the flag
-        if (lane == 0)
-          ptx::st_release_gpu(p.flags + (slot0 + static_cast<size_t>(w.split) * CG) * 4 + q,
-                              p.epoch);
+        if (lane == 0) ptx::st_release_gpu(flag(w.split), p.epoch);
         continue;
       }
       if (add_partials) {
         bool got = true;
         for (int sp = 0; sp < p.splits - 1 && got; ++sp)
-          got = wait_flag(p.flags + (slot0 + static_cast<size_t>(sp) * CG) * 4 + q, p.epoch, ctl);
+          got = wait_flag(flag(sp), p.epoch, ctl);
         if (!__all_sync(0xffffffffu, got)) break;
         // fold the other splits' partials into this accumulator (fp32)
-        for (int g = 0; g < kGroups; ++g) {
+        for (int g = g0; g < g0 + kHalfG; ++g) {
           uint32_t v[4][8];
 #pragma unroll
           for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(g) + 32 * b, v[b]);
@@ -959,36 +975,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
       }
       // Column group g (32 output columns n0 + 32g + 4k + b, k < 8, b < 4) sits in
-      // accumulator columns 128h + 32b + 8(g % 4) + k, h = g / 4.  Groups are
-      // software-pipelined: group g+1's tensor-memory loads are in flight while
-      // group g is scaled, converted and staged; two groups make one 64-column
-      // TMA store.
-      uint32_t ra[4][8], rb[4][8];
+      // accumulator columns 128h + 32b + 8(g % 4) + k, h = g / 4.  Each group is
+      // loaded, cleared, scaled, converted, staged and stored as one 32-column
+      // TMA tile; the quadrant's other epilogue warp works on the other half.
+#pragma unroll 1
+      for (int gl = 0; gl < kHalfG; ++gl) {
+        const int g = g0 + gl;
+        uint32_t cur[4][8];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(0) + 32 * b, ra[b]);
-      ptx::tmem_wait_ld();
-#pragma unroll
-      for (int g = 0; g < kGroups; ++g) {
-        uint32_t(&cur)[4][8] = (g & 1) ? rb : ra;
-        uint32_t(&nxt)[4][8] = (g & 1) ? ra : rb;
+        for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(g) + 32 * b, cur[b]);
+        ptx::tmem_wait_ld();
         // read: clear these columns for the next tile's accumulation
 #pragma unroll
         for (int b = 0; b < 4; ++b) ptx::tmem_st_32x32b_x8(gcol(g) + 32 * b, zero8);
-        if (g + 1 < kGroups) {
-#pragma unroll
-          for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(g + 1) + 32 * b, nxt[b]);
-        }
-        if ((g & 1) == 0) {
-          // the staging tile must no longer be read by its previous store
-          if (lane == 0) ptx::bulk_wait_group_read<0>();
+        if (gl + 1 == kHalfG) {
+          // this warp's columns are read and cleared: release them to the MMA
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
           __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
         }
+        // the staging tile must no longer be read by its previous store
+        if (lane == 0) ptx::bulk_wait_group_read<0>();
+        __syncwarp();
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const int o = 32 * g + 4 * k;
+          const int o = 32 * gl + 4 * k;
           const float4 wc4 = *reinterpret_cast<const float4*>(wb + o);
-          const float4 bb = *reinterpret_cast<const float4*>(wb + BN + o);
+          const float4 bb = *reinterpret_cast<const float4*>(wb + BN / 2 + o);
           const float y0 = fmaf(__uint_as_float(cur[0][k]), wc4.x, bb.x);
           const float y1 = fmaf(__uint_as_float(cur[1][k]), wc4.y, bb.y);
           const float y2 = fmaf(__uint_as_float(cur[2][k]), wc4.z, bb.z);
@@ -996,28 +1011,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[2 * k] = H::pack(y0, y1);
           pk[2 * k + 1] = H::pack(y2, y3);
         }
-        // 16-byte chunk j of the 128-byte staging row holds columns 8j .. 8j+7
+        // 16-byte chunk j of the 64-byte staging row holds columns 8j .. 8j+7
+        // (64-byte swizzle: chunk index XOR bits 1..2 of the row)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(stg + 128 * lane + (((4 * (g & 1) + j) ^ (lane & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(stg + 64 * lane + ((j ^ ((lane >> 1) & 3)) << 4)) =
               make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        if (g + 1 < kGroups) {
-          ptx::tmem_wait_ld();
-        } else {
-          // the whole accumulator is read and cleared: release it to the MMA
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
-        }
-        if (g & 1) {
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            // staging row `lane` is output row m_cta + 4 * lane + q
-            ptx::tma_store_3d(&tm_out, ptx::smem_u32(stg), n0 + 32 * (g - 1), m_cta / 4, q);
-            ptx::bulk_commit_group();
-          }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // staging row `lane` is output row m_cta + 4 * lane + q
+          ptx::tma_store_3d(&tm_out, ptx::smem_u32(stg), n0 + 32 * g, m_cta / 4, q);
+          ptx::bulk_commit_group();
         }
       }
     }
