@@ -162,6 +162,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest per-rank value over all ranks of the process group (the
+    job's step time is its slowest rank's); `x` itself without a group."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs its own full problem (weak
+    scaling), so the job does world x the work in the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def workload_inputs(synth, w, dense: bool, half: bool = False):
     """The workload's seeded inputs; the dense calibration variant drops
     wcscale and bias (the operator then uses 1 and 0) and has R = 0; the fp16
@@ -307,11 +325,7 @@ def run_ours(args, w, rank, world, local_rank):
         barrier()
         t_wall = time.perf_counter() - t_wall0
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_mean = statistics.mean(ms)
-    if dist is not None:
-        tt = torch.tensor([ms_mean], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_mean = float(tt.item())
+    ms_mean = max_over_ranks(statistics.mean(ms), dist, dev)
     code, site, _ = pkg.svdq_read_device_status(clear=True)
     if code != 0:
         raise RuntimeError(f"device status {code} at wait site {site} in the timed region")
@@ -333,16 +347,12 @@ def run_ours(args, w, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         if i >= 2:
             e_ms.append((time.perf_counter() - t0) * 1e3)
-    e_ms_mean = statistics.mean(e_ms)
-    if dist is not None:
-        tt = torch.tensor([e_ms_mean], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e_ms_mean = float(tt.item())
+    e_ms_mean = max_over_ranks(statistics.mean(e_ms), dist, dev)
 
     flops = float(w.flops)
-    tflops_kernel = flops / (ms_mean * 1e-3) / 1e12
-    value = world * tflops_kernel
-    e2e_value = world * flops / (e_ms_mean * 1e-3) / 1e12
+    tflops_kernel = job_tflops(flops, 1, ms_mean)
+    value = job_tflops(flops, world, ms_mean)
+    e2e_value = job_tflops(flops, world, e_ms_mean)
     bf16_peak, peak_src = load_peaks()
     fp4_peak = bf16_peak * NOMINAL_FP4_OVER_BF16
     traffic = committed_traffic(w.name)
