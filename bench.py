@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--dense] [--fp16] [--prepacked] [--split]
+                    [--packed-scales]
 
 One step is one operator call (the whole path: scale relayout, LoRA operand
 prep, LoRA + block-scaled MMAs, fused affine epilogue) over one synthetic
@@ -20,6 +21,9 @@ the cost of the LoRA term and the affine epilogue.  `--fp16` runs the fp16
 input/output variant (lora_up, wcscale, bias and y in IEEE fp16).
 `--prepacked` prepacks the weights once before timing (packed scale words,
 LU' = LU / wcscale, as at weight-load time) and times the prepacked call.
+`--packed-scales` additionally hands the activation scales over in the
+kernel's word layout (as an activation quantiser could write them; packed
+once before timing) and implies `--prepacked`.
 `--split` times the split-K entry point (workspace allocated once, before
 timing; the planner decides the split, e.g. on mlp_down_256x3072x12288_r128).
 """
@@ -57,6 +61,8 @@ def parse():
                     help="fp16 input/output variant (lora_up, wcscale, bias, y in fp16)")
     ap.add_argument("--prepacked", action="store_true",
                     help="weights prepacked once (svdq_prepack_weights); time the prepacked call")
+    ap.add_argument("--packed-scales", action="store_true",
+                    help="activation scales in the word layout (implies --prepacked)")
     ap.add_argument("--split", action="store_true",
                     help="time svdq_w4a4_gemm_split (planner-chosen split-K)")
     ap.add_argument("--tile-n", type=int, default=0)
@@ -272,11 +278,15 @@ def run_ours(args, w, rank, world, local_rank):
 
     inp = workload_inputs(synth, w, args.dense, args.fp16)
     d = {k: v.to(dev) for k, v in inp.items()}
+    if args.packed_scales:
+        args.prepacked = True
     if args.prepacked:
         # once per weight load, outside every timed region
         wpk, lup = pkg.svdq_prepack_weights(d["wscales"], d["lora_up"] if w.R else None,
                                             d.get("wcscale"))
         d = dict(d, wscales=wpk, lora_up=lup)
+        if args.packed_scales:
+            d["ascales"] = pkg.svdq_pack_scales(d["ascales"])
         torch.cuda.synchronize(dev)
     # what the end-to-end call copies from the host each step (the packed
     # weights when prepacked)
@@ -292,7 +302,8 @@ def run_ours(args, w, rank, world, local_rank):
                                             weights_prepacked=args.prepacked, **kw)
     out_dtype = torch.float16 if args.fp16 else torch.bfloat16
     out = torch.empty((w.M, w.N), dtype=out_dtype, device=dev)
-    opts = dict(tile_n=args.tile_n, stages=args.stages)
+    opts = dict(tile_n=args.tile_n, stages=args.stages,
+                act_scales_packed=1 if args.packed_scales else 0)
     plan = pkg.svdq_query_plan(w.M, w.N, w.K, w.R,
                                options=dict(opts, k_splits=-1) if args.split else opts)
     stream = torch.cuda.current_stream(dev)
@@ -406,14 +417,16 @@ def main():
     from nvfp4_w4a4_quantized_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
-    if args.dense or args.fp16 or args.prepacked or args.split:
+    if args.dense or args.fp16 or args.prepacked or args.split or args.packed_scales:
         import dataclasses
 
         if args.dense:
             w = dataclasses.replace(w, name=w.name + "_dense", R=0)
         if args.fp16:
             w = dataclasses.replace(w, name=w.name + "_fp16")
-        if args.prepacked:
+        if args.packed_scales:
+            w = dataclasses.replace(w, name=w.name + "_packed_scales")
+        elif args.prepacked:
             w = dataclasses.replace(w, name=w.name + "_prepacked")
         if args.split:
             w = dataclasses.replace(w, name=w.name + "_split")

@@ -113,6 +113,11 @@ typedef struct svdq_options {
                             workspace, the planner's choice on svdq_w4a4_gemm_split);
                             -1 = the planner's choice; 1 = none; 2..8 = that many K
                             splits per tile (svdq_w4a4_gemm_split only)           */
+    int32_t act_scales_packed; /* 0 = ascales as uint8 [K/16, M] (default); 1 = the
+                            same scales as uint32 words [K/64, M], word (s, m) byte g
+                            = ascales[4s + g][m] (svdq_pack_scales' layout): an
+                            activation quantiser that writes them this way saves
+                            the kernel's per-call transpose                      */
 } svdq_options_t;
 
 /* svdq_w4a4_gemm with options; identical semantics otherwise.  With
@@ -155,6 +160,18 @@ int svdq_w4a4_gemm_ex(const void* act, const void* wgt, const void* ascales, con
 int svdq_prepack_weights(const void* wscales, const void* lora_up, const void* wcscale,
                          int64_t N, int64_t K, int64_t R, int32_t io_dtype, void* wscales_packed,
                          void* lora_up_packed, void* stream);
+
+/*
+ * svdq_pack_scales -- any FP8-E4M3 scale tensor [K/16, rows] (activation or
+ * weight scales) into the word layout the kernel feeds to the tensor core
+ * ("SVDQuant W4A4 on Blackwell" §3.1: one 32-bit word of four group scales
+ * per row and 64-wide K step): uint32 [K/64, rows], word (s, r) byte g =
+ * scales[4s + g][r].  The words are what svdq_options_t.act_scales_packed
+ * expects for ascales and what svdq_prepack_weights writes for wscales.
+ * rows a multiple of 16, K of 64; 16-byte aligned pointers; asynchronous on
+ * `stream`, allocates nothing.  Returns SVDQ_OK for rows == 0.
+ */
+int svdq_pack_scales(const void* scales, int64_t rows, int64_t K, void* packed, void* stream);
 
 /*
  * svdq_w4a4_gemm_prepacked -- svdq_w4a4_gemm_ex on prepacked weights: the

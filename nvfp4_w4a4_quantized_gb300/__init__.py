@@ -10,6 +10,6 @@ point names, and the seeded synthetic input generator.
 from .binding import (SVDQ_ERR_BAD_OPTION, SVDQ_ERR_INVALID_ARG, SVDQ_ERR_MISALIGNED,  # noqa: F401
                       SVDQ_ERR_TIMEOUT, SVDQ_ERR_UNSUPPORTED_DEVICE, SVDQ_ERR_UNSUPPORTED_SHAPE,
                       SVDQ_OK, SvdqError, SvdqOptions, load, status_string, svdq_lora_stage_bytes,
-                      svdq_prepack_weights, svdq_query_plan, svdq_read_device_status,
+                      svdq_pack_scales, svdq_prepack_weights, svdq_query_plan, svdq_read_device_status,
                       svdq_version, svdq_w4a4_gemm, svdq_w4a4_gemm_prepacked,
                       svdq_w4a4_gemm_split, svdq_workspace_size)

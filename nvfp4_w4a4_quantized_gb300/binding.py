@@ -32,7 +32,7 @@ SVDQ_IO_BF16 = 0
 SVDQ_IO_FP16 = 1
 
 # Every symbol include/svdq.h declares.
-EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_prepack_weights",
+EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_prepack_weights", "svdq_pack_scales",
             "svdq_w4a4_gemm_prepacked", "svdq_w4a4_gemm_split", "svdq_w4a4_gemm_split_noalloc",
             "svdq_workspace_size",
             "svdq_query_plan", "svdq_lora_stage_bytes", "svdq_read_device_status",
@@ -43,7 +43,8 @@ class SvdqOptions(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("debug_fault", ctypes.c_int32), ("cta_group", ctypes.c_int32),
-                ("io_dtype", ctypes.c_int32), ("k_splits", ctypes.c_int32)]
+                ("io_dtype", ctypes.c_int32), ("k_splits", ctypes.c_int32),
+                ("act_scales_packed", ctypes.c_int32)]
 
 
 class SvdqPlan(ctypes.Structure):
@@ -95,6 +96,8 @@ def load(path: Optional[str] = None):
         lib.svdq_w4a4_gemm_ex.argtypes = [vp] * 9 + [i64] * 4 + [ctypes.POINTER(SvdqOptions), vp]
         lib.svdq_prepack_weights.restype = ctypes.c_int
         lib.svdq_prepack_weights.argtypes = [vp] * 3 + [i64] * 3 + [i32] + [vp] * 3
+        lib.svdq_pack_scales.restype = ctypes.c_int
+        lib.svdq_pack_scales.argtypes = [vp, i64, i64, vp, vp]
         lib.svdq_w4a4_gemm_prepacked.restype = ctypes.c_int
         lib.svdq_w4a4_gemm_prepacked.argtypes = ([vp] * 9 + [i64] * 4 +
                                                  [ctypes.POINTER(SvdqOptions), vp])
@@ -220,14 +223,17 @@ def _gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, 
     h16 = torch.float16 if out.dtype == torch.float16 else torch.bfloat16
     ws_dt = torch.int32 if prepacked else torch.uint8
     ws_shape = (K // 64, N) if prepacked else (K // 16, N)
+    act_packed = bool(_opts(options) and _opts(options).act_scales_packed)
+    as_dt = torch.int32 if act_packed else torch.uint8
+    as_shape = (K // 64, M) if act_packed else (K // 16, M)
     for name, t, dt in (("act", act, torch.uint8), ("wgt", wgt, torch.uint8),
-                        ("ascales", ascales, torch.uint8), ("wscales", wscales, ws_dt),
+                        ("ascales", ascales, as_dt), ("wscales", wscales, ws_dt),
                         ("lora_act_in", lora_act_in, torch.float32),
                         ("lora_up", lora_up if R else None, h16), ("wcscale", wcscale, h16),
                         ("bias", bias, h16), ("out", out, h16)):
         if t is not None:
             _check(name, t, dt)
-    if tuple(wgt.shape) != (N, kh) or tuple(ascales.shape) != (K // 16, M) or \
+    if tuple(wgt.shape) != (N, kh) or tuple(ascales.shape) != as_shape or \
             tuple(wscales.shape) != ws_shape or tuple(out.shape) != (M, N):
         raise ValueError("inconsistent operand shapes")
     if R and (lora_up is None or tuple(lora_up.shape) != (N, R)):
@@ -261,6 +267,28 @@ def _gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, 
         raise SvdqError(rc, "svdq_w4a4_gemm_split" if workspace is not None else
                         "svdq_w4a4_gemm_prepacked" if prepacked else "svdq_w4a4_gemm")
     return rc
+
+
+def svdq_pack_scales(scales, packed=None, stream=None, check: bool = True):
+    """Scale tensor uint8 [K/16, rows] -> uint32 words [K/64, rows] (returned
+    as int32; allocated here unless given): the layout act_scales_packed
+    expects for ascales and svdq_prepack_weights writes for wscales."""
+    import torch
+
+    _check("scales", scales, torch.uint8)
+    G, rows = scales.shape
+    K = 16 * G
+    if K % 64:
+        raise ValueError("K must be a multiple of 64")
+    if packed is None:
+        packed = torch.empty((K // 64, rows), dtype=torch.int32, device=scales.device)
+    _check("packed", packed, torch.int32)
+    h = _stream_handle(stream, scales.device)
+    with torch.cuda.device(scales.device):
+        rc = load().svdq_pack_scales(_ptr(scales), rows, K, _ptr(packed), h)
+    if check and rc != SVDQ_OK:
+        raise SvdqError(rc, "svdq_pack_scales")
+    return packed
 
 
 def svdq_prepack_weights(wscales, lora_up, wcscale, wscales_packed=None, lora_up_packed=None,

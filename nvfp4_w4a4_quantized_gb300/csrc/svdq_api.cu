@@ -87,6 +87,7 @@ int validate_options(const svdq_options_t* o) {
   if (o->cta_group == 2 && o->tile_n == 128) return SVDQ_ERR_BAD_OPTION;
   if (o->io_dtype != SVDQ_IO_BF16 && o->io_dtype != SVDQ_IO_FP16) return SVDQ_ERR_BAD_OPTION;
   if (o->k_splits < -1 || o->k_splits > kMaxSplits) return SVDQ_ERR_BAD_OPTION;
+  if (o->act_scales_packed != 0 && o->act_scales_packed != 1) return SVDQ_ERR_BAD_OPTION;
   return SVDQ_OK;
 }
 
@@ -385,12 +386,22 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
     if ((rc = encode(&tm[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, op.wgt, d_wgt, s_act, b_quad,
                      CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
       return rc;
-    const uint64_t d_sfa[2] = {static_cast<uint64_t>(M), static_cast<uint64_t>(K / 16)},
-                   s_sfa[1] = {static_cast<uint64_t>(M)};
-    const uint32_t b_sfa[2] = {kBM, 16 * KBI};
-    if ((rc = encode(&tm[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.ascales, d_sfa, s_sfa, b_sfa,
-                     CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
-      return rc;
+    if (kp.act_packed) {
+      // packed activation scale words uint32 [K/64][M]: 16 * kBM bytes per K block
+      const uint64_t d_sfa[2] = {static_cast<uint64_t>(M), static_cast<uint64_t>(K / 64)},
+                     s_sfa[1] = {static_cast<uint64_t>(M) * 4};
+      const uint32_t b_sfa[2] = {kBM, 4 * KBI};
+      if ((rc = encode(&tm[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, op.ascales, d_sfa, s_sfa,
+                       b_sfa, CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
+        return rc;
+    } else {
+      const uint64_t d_sfa[2] = {static_cast<uint64_t>(M), static_cast<uint64_t>(K / 16)},
+                     s_sfa[1] = {static_cast<uint64_t>(M)};
+      const uint32_t b_sfa[2] = {kBM, 16 * KBI};
+      if ((rc = encode(&tm[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, op.ascales, d_sfa, s_sfa, b_sfa,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) != SVDQ_OK)
+        return rc;
+    }
     if (kp.prepacked) {
       // packed scale words uint32 [K/64][N]: the same 16 * BN bytes per K block
       const uint64_t d_sfb[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K / 64)},
@@ -569,12 +580,14 @@ int run_gemm(const void* act, const void* wgt, const void* ascales, const void* 
   kp.num_stages = pl.stages;
   kp.lora_tma = (R > 0 && R % 8 == 0);
   kp.prepacked = prepacked ? 1 : 0;
+  kp.act_packed = (options != nullptr && options->act_scales_packed) ? 1 : 0;
   kp.splits = pl.splits;
   kp.num_units = static_cast<int>(pl.num_units);
   if (pl.splits > 1) {
     if (!aligned(workspace, kWsAlign) || workspace_bytes < ws_bytes(pl)) return SVDQ_ERR_WORKSPACE;
     kp.partials = static_cast<float4*>(workspace);
-    kp.flags = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + ws_flag_offset(pl));
+    kp.flags =
+        reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + ws_flag_offset(pl));
     kp.epoch = next_epoch();
   }
   kp.debug_fault = options ? options->debug_fault : 0;
@@ -651,6 +664,31 @@ extern "C" int64_t svdq_workspace_size(int64_t M, int64_t N, int64_t K, int64_t 
     return rc;
   }
   return ws_bytes(pl);
+}
+
+extern "C" int svdq_pack_scales(const void* scales, int64_t rows, int64_t K, void* packed,
+                                void* stream) {
+  if (rows < 0 || K <= 0) return SVDQ_ERR_INVALID_ARG;
+  if (rows % 16 || K % 64 || rows > SVDQ_MAX_MN || K > SVDQ_MAX_K)
+    return SVDQ_ERR_UNSUPPORTED_SHAPE;
+  if (!scales || !packed) return SVDQ_ERR_INVALID_ARG;
+  if (!aligned(scales, 16) || !aligned(packed, 16)) return SVDQ_ERR_MISALIGNED;
+  if (rows == 0) return SVDQ_OK;
+  int dev = 0;
+  DeviceInfo* dinfo = nullptr;
+  int rc = probe_device(&dev, &dinfo);
+  if (rc != SVDQ_OK) return rc;
+  const long long work = (K / 64) * (rows / 4);
+  long long blocks = (work + 255) / 256;
+  const long long cap = 8LL * dinfo->sm_count;
+  if (blocks > cap) blocks = cap;
+  // the weight prepack kernel with no LoRA operand: its scale-word pass only
+  svdq_prepack_kernel<false><<<static_cast<unsigned>(blocks), 256, 0,
+                               static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint8_t*>(scales), nullptr, nullptr, static_cast<uint32_t*>(packed),
+      nullptr, static_cast<int>(rows), static_cast<int>(K), 0);
+  if (cudaGetLastError() != cudaSuccess) return SVDQ_ERR_LAUNCH;
+  return SVDQ_OK;
 }
 
 extern "C" int svdq_prepack_weights(const void* wscales, const void* lora_up,

@@ -170,6 +170,7 @@ struct KParams {
   int num_stages;
   int lora_tma;     // R % 8 == 0: LoRA rows arrive by TMA; else direct loads
   int prepacked;    // weights prepacked: scale words [K/64][N], lora_up = LU'
+  int act_packed;   // activation scales arrive as words [K/64][M]
   int splits;       // K splits per tile (1: every unit is a whole tile)
   int num_units;    // num_tiles * splits
   unsigned int epoch;     // split-K: the value this launch's flags are raised to
@@ -619,8 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nkb = min(KBI, p.k_blocks - kb0);
             if (role == 0) {
               ptx::mbar_arrive_expect_tx(ab, main_aux_bytes);
-              ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, ab, m_cta, kb0 * 16);
               // raw scales: 16 group rows per K block; packed words: 4 step rows
+              ptx::tma_load_2d(st + L::kOffSFA, &tm_sfa, ab, m_cta,
+                               kb0 * (p.act_packed ? 4 : 16));
               ptx::tma_load_2d(st + L::kOffSFB, &tm_sfb, ab, n0, kb0 * (p.prepacked ? 4 : 16));
               // The act / wgt loads of this item may land before this count
               // (the transaction count runs negative meanwhile); the phase
@@ -1062,17 +1064,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the block-scaled MMA reads the scale words in every quadrant.
           const uint32_t col = tmem_base + lane_base +
                                static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
-          // Prepacked weight scales arrive as words [step][BN]: lane a's four
-          // words of a 128-column half are 16 consecutive bytes.
-          auto feed = [&](auto packed_tag) {
+          // Packed scales arrive as words [step][rows]: lane a's four words of a
+          // 128-row block are 16 consecutive bytes (weights: prepacked;
+          // activations: act_scales_packed).
+          auto feed = [&](auto packed_tag, auto act_tag) {
             constexpr bool kPacked = decltype(packed_tag)::value;
+            constexpr bool kActPacked = decltype(act_tag)::value;
 #pragma unroll
             for (int kk = 0; kk < KBI; ++kk) {
               uint32_t a[16], b[16 * L::kSfbHalves];
 #pragma unroll
               for (int s4 = 0; s4 < 4; ++s4) {
                 const int ks = 4 * kk + s4;
-                sf_words(st + L::kOffSFA + 4 * kBM * ks, kBM, lane, a + 4 * s4);
+                if (kActPacked) {
+                  const uint4 va = lds128(st + L::kOffSFA + 4 * kBM * ks + 16 * lane);
+                  a[4 * s4] = va.x;
+                  a[4 * s4 + 1] = va.y;
+                  a[4 * s4 + 2] = va.z;
+                  a[4 * s4 + 3] = va.w;
+                } else {
+                  sf_words(st + L::kOffSFA + 4 * kBM * ks, kBM, lane, a + 4 * s4);
+                }
 #pragma unroll
                 for (int h = 0; h < L::kSfbHalves; ++h) {
                   uint32_t* bw = b + 4 * (s4 * L::kSfbHalves + h);
@@ -1108,10 +1120,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           };
-          if (p.prepacked)
-            feed(std::true_type{});
-          else
-            feed(std::false_type{});
+          if (p.prepacked) {
+            if (p.act_packed)
+              feed(std::true_type{}, std::true_type{});
+            else
+              feed(std::true_type{}, std::false_type{});
+          } else if (p.act_packed) {
+            feed(std::false_type{}, std::true_type{});
+          } else {
+            feed(std::false_type{}, std::false_type{});
+          }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
         }

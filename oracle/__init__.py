@@ -6,6 +6,6 @@ Only tests/, the package's smoke check and bench.py's CPU-baseline leg may
 import it.
 """
 
-from .prepack_ref import prepack_lora_up, prepack_wscales  # noqa: F401
+from .prepack_ref import pack_scales, prepack_lora_up, prepack_wscales  # noqa: F401
 from .svdq_ref import (bf16_value, build, e2m1, e4m3, f16_value, forward,  # noqa: F401
                        num_threads, round_bf16_bits)

@@ -24,15 +24,21 @@ import numpy as np
 from .svdq_ref import _np_bytes
 
 
-def prepack_wscales(wscales, N: int, K: int) -> np.ndarray:
-    """uint32 [K/64][N]: word (s, n) byte g = wscales[4s + g][n]."""
+def pack_scales(scales, rows: int, K: int) -> np.ndarray:
+    """Any scale tensor [K/16][rows] (activations or weights) as uint32
+    [K/64][rows]: word (s, r) byte g = scales[4s + g][r]."""
     if K % 64:
         raise ValueError("K must be a multiple of 64")
-    w = _np_bytes(wscales, np.uint8).reshape(K // 16, N).astype(np.uint32)
-    out = np.zeros((K // 64, N), dtype=np.uint32)
+    w = _np_bytes(scales, np.uint8).reshape(K // 16, rows).astype(np.uint32)
+    out = np.zeros((K // 64, rows), dtype=np.uint32)
     for g in range(4):
         out |= w[g::4, :] << np.uint32(8 * g)
     return out
+
+
+def prepack_wscales(wscales, N: int, K: int) -> np.ndarray:
+    """uint32 [K/64][N]: word (s, n) byte g = wscales[4s + g][n]."""
+    return pack_scales(wscales, N, K)
 
 
 def _decode16(bits: np.ndarray, half: bool) -> np.ndarray:

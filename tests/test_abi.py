@@ -92,6 +92,7 @@ def call(lib, M=256, N=256, K=256, R=32, ptrs=None, opts=None, prepacked=False):
     (dict(opts=dict(debug_fault=2)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(k_splits=9)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(k_splits=-2)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(act_scales_packed=2)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(io_dtype=2)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(cta_group=3)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(cta_group=2, tile_n=128)), binding.SVDQ_ERR_BAD_OPTION),
@@ -264,3 +265,16 @@ def test_split_plan_forced_and_rejected(lib):
     with pytest.raises(binding.SvdqError) as e:
         binding.svdq_query_plan(4096, 3072, 3072, 32, options=dict(k_splits=2), sm_count=SMS)
     assert e.value.status == binding.SVDQ_ERR_BAD_OPTION
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A, 40, 256, A), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    ((A, 256, 96, A), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    ((A, -16, 256, A), binding.SVDQ_ERR_INVALID_ARG),
+    ((None, 256, 256, A), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, 256, 256, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((A + 4, 256, 256, A), binding.SVDQ_ERR_MISALIGNED),
+    ((A, 0, 256, A), binding.SVDQ_OK),
+])
+def test_pack_scales_host_validation(lib, args, expect):
+    assert lib.svdq_pack_scales(*args, None) == expect

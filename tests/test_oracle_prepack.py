@@ -144,3 +144,13 @@ def test_lu_prime_zero_wcscale_gives_zero():
     assert not (got[5] & 0x7FFF).any()  # +0 or -0 (the sign of LU times zero)
     assert got[4].any()
     assert math.isfinite(oracle.bf16_value(int(got[4, 0])))
+
+
+@pytest.mark.parametrize("rows,K", [(16, 64), (272, 1088), (4096, 3072)])
+def test_packed_activation_scales_read_back_as_bytes(rows, K):
+    # the same word layout for activation scales [K/16][M]
+    rng = np.random.default_rng(rows + K + 1)
+    sc = rng.integers(0, 256, size=(K // 16, rows), dtype=np.uint8)
+    pk = oracle.pack_scales(sc, rows, K)
+    by = pk.astype("<u4").view(np.uint8).reshape(K // 64, rows, 4)
+    assert np.array_equal(np.transpose(by, (0, 2, 1)).reshape(K // 16, rows), sc)
