@@ -14,12 +14,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t l;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-  return l;
-}
-
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -116,10 +110,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // ---------------------------------------------------------------- TMEM
 // Warp-collective: allocate ncols (power of two >= 32) tensor-memory columns
 // and write the base address to shared memory at dst.
@@ -162,12 +152,6 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
 // (512 bytes) are contiguous.
 __device__ __forceinline__ uint64_t desc_kmajor_sw64(uint32_t saddr) {
   return smem_desc(saddr, 16, 512, 4);
-}
-
-// Scale-factor block for tcgen05.cp .32x128b: 32 rows of 16 bytes, no swizzle,
-// 8-row core groups 128 bytes apart.
-__device__ __forceinline__ uint64_t desc_sf_32x16(uint32_t saddr) {
-  return smem_desc(saddr, 0, 128, 0);
 }
 
 // Instruction descriptor, block-scaled kinds (mxf4nvf4): B scale-factor id in
@@ -220,28 +204,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Copy 32 rows x 128 bits from shared memory into tensor memory (4 columns),
-// replicated into all four 32-lane quadrants.
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-               : "memory");
-}
-
-// Warp-collective: 32 lanes x 32 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
-      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
-      " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
-
 // Warp-collective: 32 lanes x 8 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t* r) {
   asm volatile(
@@ -281,18 +243,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
-// Bounded-wait building block with cluster-scope acquire (remote arrivals).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 // ---------------------------------------------------------------- TMA (more forms)
 // 1-D tiled load (a box of consecutive elements).
@@ -302,23 +252,6 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* tmap, uint
       " [%0], [%1, {%3}], [%2];" ::"r"(dst),
       "l"(tmap), "r"(bar), "r"(x)
       : "memory");
-}
-// 2-D tiled load whose completion is signalled on an mbarrier that may live in
-// the peer CTA of a CTA pair (cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, uint32_t cluster_bar,
-                                                 int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(tmap), "r"(cluster_bar), "r"(x), "r"(y)
-      : "memory");
-}
-// 2-D tiled store shared -> global (bulk-group completion).
-__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   tmap),
-               "r"(src), "r"(x), "r"(y)
-               : "memory");
 }
 // 3-D forms (x innermost).  Used with row-quad tensor maps whose second
 // dimension steps four rows and whose third steps one row.
@@ -439,12 +372,6 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
 }
 
 // ---------------------------------------------------------------- misc
-__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
 // Acquire load / release store of a global word, GPU scope.
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
   unsigned int v;
