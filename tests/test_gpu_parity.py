@@ -196,6 +196,15 @@ def test_workload_sampled_rows(w, cfg):
     parity(y[rows], ref)
 
 
+@pytest.mark.parametrize("w", [synth.ATTN_PROJ, synth.MLP_UP, synth.MLP_DOWN], ids=lambda w: w.name)
+def test_workload_full_matrix(w):
+    # every element of the full-size workload, in the launch configuration the
+    # bench times (the oracle takes 2 to 10 s of host time per workload)
+    inp = synth.make_workload_inputs(w)
+    y = run_gpu(inp, w.M, w.N, w.K, w.R)
+    parity(y, oracle_y(inp, w.M, w.N, w.K, w.R))
+
+
 @pytest.mark.parametrize("w", synth.sweep_workloads(), ids=lambda w: w.name)
 def test_sweep_sampled_rows(w):
     inp = synth.make_workload_inputs(w)
