@@ -34,6 +34,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -82,13 +83,23 @@ def load_peaks():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def _code_only(src: str) -> str:
+    """C++ source without comments and with whitespace collapsed (string
+    literals in these files hold no comment markers)."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_hash() -> str:
+    """Identifies the kernel code the committed ncu counters were taken on;
+    comment edits do not change it."""
     h = hashlib.sha256()
     for rel in ("nvfp4_w4a4_quantized_gb300/csrc/svdq_kernel.cuh",
                 "nvfp4_w4a4_quantized_gb300/csrc/ptx.cuh",
                 "nvfp4_w4a4_quantized_gb300/csrc/svdq_api.cu"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,9 +9,11 @@
 // affine epilogue).
 //
 // Template parameters: CG = CTAs per MMA (1, or 2 for a CTA pair issuing
-// cta_group::2 MMAs of M = 256), BN = output columns per tile.  Each CTA owns
-// 128 output rows; in a pair the leader (cluster rank 0) issues every MMA,
-// A is split along M and B along N between the two CTAs' shared memory.
+// cta_group::2 MMAs of M = 256), BN = output columns per tile, KBI = K blocks
+// per ring item (1), F16 = fp16 instead of bf16 16-bit I/O, SK = split-K
+// instance.  Each CTA owns 128 output rows; in a pair the leader (cluster
+// rank 0) issues every MMA, A is split along M and B along N between the two
+// CTAs' shared memory.
 //
 // Row-quad order.  Inside every 128-row block of an operand tile, tile row
 // a + 32b (a < 32, b < 4) holds matrix row 4a + b.  The TMA builds this order
@@ -49,16 +51,20 @@
 //                last group (the MMA waits for all eight).
 //   warps 8..11  scale feeders: turn the stage's scale boxes into row-per-lane
 //                words in registers (a 4x4 byte transpose of raw scales, or
-//                plain 16-byte loads of prepacked weight-scale words) and write
+//                plain 16-byte loads of scale words: prepacked weights,
+//                activation scales handed over packed) and write
 //                them into tensor memory with tcgen05.st (one warp per 32-lane
 //                quadrant), off the MMA pipe; on LoRA items they build
 //                LA' = round16(LA), 32 rows each.
 // Warp w accesses tensor-memory lanes 32(w%4) .. 32(w%4)+31, so epilogue warps
 // 4..7 and 15..18 and scale feeders 8..11 each cover all four quadrants.
 //
-// Per output tile the ring carries ceil(R/32) LoRA items, then ceil(K/256)
-// main items; every role walks the same item sequence, so stage index and
-// phase bit survive tile boundaries.  Every MMA accumulates into an
+// Per unit of work (an output tile, or with split-K one of its K ranges) the
+// ring carries ceil(R/32) LoRA items (on the first split only), then its main
+// items; every role walks the same item sequence, so stage index and phase
+// bit survive unit boundaries.  Split-K units that are not a tile's last split
+// store an fp32 partial tile and raise a per-launch flag; the last split adds
+// them in tensor memory before its epilogue.  Every MMA accumulates into an
 // accumulator the epilogue has cleared, so the LoRA and block-scaled MMAs of
 // the two issuers may reach the tensor core in any order.  LU' is pre-divided
 // by wcscale, so the epilogue's acc * wcscale restores LA @ LU unscaled, as the
