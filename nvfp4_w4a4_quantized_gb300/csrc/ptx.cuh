@@ -372,6 +372,15 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
 }
 
 // ---------------------------------------------------------------- misc
+// Programmatic dependent launch: wait until the previous grid in the stream
+// has completed (its memory visible); allow this grid's dependents to launch.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Acquire load / release store of a global word, GPU scope.
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
   unsigned int v;

@@ -455,13 +455,17 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = pl.smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CG;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  // the kernel waits (griddepcontrol.wait) before touching memory, so it may
+  // be scheduled while the previous kernel in the stream finishes
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CG;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = CG == 2 ? 1 : 0;
+  cfg.numAttrs = CG == 2 ? 2 : 1;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, svdq_w4a4_kernel<CG, BN, KBI, F16, SK>, tm[0], tm[1], tm[2],
                          tm[3], tm[4], tm[5], tm[6], tm[7], kp);

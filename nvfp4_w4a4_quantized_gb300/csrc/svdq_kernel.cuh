@@ -568,6 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (CG == 2) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // Launched with programmatic stream serialisation: the set-up above may
+  // overlap the tail of the previous kernel in the stream, but no global
+  // memory is read or written before that kernel has completed.  Kernels
+  // launched after this one may be scheduled from here on (they wait the same
+  // way before touching memory).
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   if (warp == 0 || warp == 12 || warp == 13) {
     // ------------------------------------------------------------ producers
