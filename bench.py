@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--dense] [--fp16] [--prepacked] [--split]
-                    [--packed-scales]
+                    [--packed-scales] [--relaxed-order]
 
 One step is one operator call (the whole path: scale relayout, LoRA operand
 prep, LoRA + block-scaled MMAs, fused affine epilogue) over one synthetic
@@ -26,6 +26,8 @@ kernel's word layout (as an activation quantiser could write them; packed
 once before timing) and implies `--prepacked`.
 `--split` times the split-K entry point (workspace allocated once, before
 timing; the planner decides the split, e.g. on mlp_down_256x3072x12288_r128).
+Calls are bit-reproducible by default (the MMA issuers take turns);
+`--relaxed-order` times svdq_options_t.relaxed_order = 1 instead.
 """
 
 from __future__ import annotations
@@ -66,6 +68,8 @@ def parse():
                     help="activation scales in the word layout (implies --prepacked)")
     ap.add_argument("--split", action="store_true",
                     help="time svdq_w4a4_gemm_split (planner-chosen split-K)")
+    ap.add_argument("--relaxed-order", action="store_true",
+                    help="relaxed_order = 1: MMA issue order free, output bits may vary")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -314,7 +318,8 @@ def run_ours(args, w, rank, world, local_rank):
     out_dtype = torch.float16 if args.fp16 else torch.bfloat16
     out = torch.empty((w.M, w.N), dtype=out_dtype, device=dev)
     opts = dict(tile_n=args.tile_n, stages=args.stages,
-                act_scales_packed=1 if args.packed_scales else 0)
+                act_scales_packed=1 if args.packed_scales else 0,
+                relaxed_order=1 if args.relaxed_order else 0)
     plan = pkg.svdq_query_plan(w.M, w.N, w.K, w.R,
                                options=dict(opts, k_splits=-1) if args.split else opts)
     stream = torch.cuda.current_stream(dev)
@@ -455,7 +460,9 @@ def run_ours(args, w, rank, world, local_rank):
                        "l2": "flushed: 256 MiB memset before every timed launch",
                        "parallelism": f"replicas x{world} (independent problems, no collective)",
                        "tile": [plan["tile_m"], plan["tile_n"]], "stages": plan["num_ab_stage"],
-                       "grid": plan["grid"], "k_splits": plan["k_splits"]},
+                       "grid": plan["grid"], "k_splits": plan["k_splits"],
+                       "mma_order": "relaxed" if args.relaxed_order else
+                                    "ring order (bit-reproducible)"},
             "mfu_vs_10pf": tflops_kernel / BASELINE_PEAK_TFLOPS,
             "ms_per_step_min": min(ms), "ms_per_step_median": statistics.median(ms),
             "wall_s_timed_region": t_wall,
@@ -489,7 +496,8 @@ def main():
     from nvfp4_w4a4_quantized_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
-    if args.dense or args.fp16 or args.prepacked or args.split or args.packed_scales:
+    if (args.dense or args.fp16 or args.prepacked or args.split or args.packed_scales
+            or args.relaxed_order):
         import dataclasses
 
         if args.dense:
@@ -502,6 +510,8 @@ def main():
             w = dataclasses.replace(w, name=w.name + "_prepacked")
         if args.split:
             w = dataclasses.replace(w, name=w.name + "_split")
+        if args.relaxed_order:
+            w = dataclasses.replace(w, name=w.name + "_relaxed_order")
     if args.impl == "reference":
         run_reference(args, w, rank)
     else:

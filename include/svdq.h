@@ -86,8 +86,9 @@ extern "C" {
  * and allocates no device memory.  Inputs must not be modified and `out`
  * must not be read until the stream reaches the call.  `out` must not
  * overlap any input.  Accumulation is fp32 in tensor memory; the result is
- * rounded to bf16 once.  The call is thread-safe; concurrent calls on
- * different streams are independent.
+ * rounded to bf16 once, and the same call on the same inputs and device gives
+ * the same bits (see svdq_options_t.relaxed_order).  The call is thread-safe;
+ * concurrent calls on different streams are independent.
  */
 int svdq_w4a4_gemm(const void* act, const void* wgt, const void* ascales, const void* wscales,
                    const float* lora_act_in, const void* lora_up, const void* wcscale,
@@ -118,6 +119,14 @@ typedef struct svdq_options {
                             = ascales[4s + g][m] (svdq_pack_scales' layout): an
                             activation quantiser that writes them this way saves
                             the kernel's per-call transpose                      */
+    int32_t relaxed_order; /* 0 = bit-reproducible (default): the two MMA issuer
+                            threads take turns, so ring items reach the tensor core
+                            in a fixed order and every call on the same inputs gives
+                            the same bits; 1 = the issuers run freely, so the fp32
+                            accumulation order (and the last bits of out, always
+                            within the stated tolerance) may change from call to
+                            call, for a few percent more speed when scales arrive
+                            packed                                               */
 } svdq_options_t;
 
 /* svdq_w4a4_gemm with options; identical semantics otherwise.  With

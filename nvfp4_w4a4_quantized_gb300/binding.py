@@ -44,7 +44,7 @@ class SvdqOptions(ctypes.Structure):
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("debug_fault", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("io_dtype", ctypes.c_int32), ("k_splits", ctypes.c_int32),
-                ("act_scales_packed", ctypes.c_int32)]
+                ("act_scales_packed", ctypes.c_int32), ("relaxed_order", ctypes.c_int32)]
 
 
 class SvdqPlan(ctypes.Structure):

@@ -88,6 +88,7 @@ int validate_options(const svdq_options_t* o) {
   if (o->io_dtype != SVDQ_IO_BF16 && o->io_dtype != SVDQ_IO_FP16) return SVDQ_ERR_BAD_OPTION;
   if (o->k_splits < -1 || o->k_splits > kMaxSplits) return SVDQ_ERR_BAD_OPTION;
   if (o->act_scales_packed != 0 && o->act_scales_packed != 1) return SVDQ_ERR_BAD_OPTION;
+  if (o->relaxed_order != 0 && o->relaxed_order != 1) return SVDQ_ERR_BAD_OPTION;
   return SVDQ_OK;
 }
 
@@ -595,6 +596,7 @@ int run_gemm(const void* act, const void* wgt, const void* ascales, const void* 
     kp.epoch = next_epoch();
   }
   kp.debug_fault = options ? options->debug_fault : 0;
+  kp.ordered = (options != nullptr && options->relaxed_order) ? 0 : 1;
   const int tmo = (options && options->timeout_ms) ? options->timeout_ms : kDefaultTimeoutMs;
   kp.timeout_ns = static_cast<unsigned long long>(tmo) * 1000000ull;
   kp.lora_act_in = R > 0 ? lora_act_in : nullptr;

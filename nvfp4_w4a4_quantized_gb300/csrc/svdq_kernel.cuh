@@ -65,8 +65,9 @@
 // bit survive unit boundaries.  Split-K units that are not a tile's last split
 // store an fp32 partial tile and raise a per-launch flag; the last split adds
 // them in tensor memory before its epilogue.  Every MMA accumulates into an
-// accumulator the epilogue has cleared, so the LoRA and block-scaled MMAs of
-// the two issuers may reach the tensor core in any order.  LU' is pre-divided
+// accumulator the epilogue has cleared, so no LoRA or block-scaled MMA waits
+// for another to complete; the two issuers take turns, so items reach the
+// tensor core in ring order and results are bit-reproducible.  LU' is pre-divided
 // by wcscale, so the epilogue's acc * wcscale restores LA @ LU unscaled, as the
 // operator states.
 //
@@ -101,6 +102,7 @@ enum WaitSite : int {
   kSiteProducerEmpty = 1,
   kSiteMmaAccEmpty = 2,
   kSiteMmaFull = 3,
+  kSiteMmaTurn = 5,
   kSiteLoraAuxFull = 6,
   kSiteSfAuxFull = 7,
   kSiteEpiAccFull = 8,
@@ -183,6 +185,7 @@ struct KParams {
   float4* partials;       // split-K: fp32 partial tiles of the non-final splits
   unsigned int* flags;    // split-K: one per (tile, non-final split, CTA, epilogue warp)
   int debug_fault;
+  int ordered;  // the MMA issuers take turns: bit-reproducible accumulation order
   unsigned long long timeout_ns;
   const float* lora_act_in;
   const uint16_t* lora_up;  // bf16 or fp16 bits (the kernel's 16-bit I/O type)
@@ -305,6 +308,35 @@ __device__ __forceinline__ bool wait_flag(const unsigned int* f, unsigned int v,
       return false;
     }
   }
+}
+
+// Bounded wait until the turn word (a shared-memory address) reaches v: the
+// other MMA issuer has issued the MMAs of item v - 1.  The slow path of
+// wait_turn, kept out of line: code inlined into the issuers' loop slows
+// every ring item, even where it never runs.  The abort flag and the time
+// limit are checked every 64 polls.
+__device__ __noinline__ bool wait_turn_slow(uint32_t turn, uint32_t v, const Ctl& c) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int n = 0; n < 64; ++n)
+      if (ptx::ld_volatile_shared(turn) == v) return true;
+    if (*c.abort_flag) return false;
+    if (ptx::globaltimer() - t0 > c.timeout_ns) {
+      *c.abort_flag = 1;
+      report_timeout(c.status, kSiteMmaTurn);
+      return false;
+    }
+  }
+}
+
+// The usual hand-off takes a few polls: spin briefly inline, then fall back
+// to the bounded wait.
+__device__ __forceinline__ bool wait_turn(uint32_t turn, uint32_t v, const Ctl& c) {
+#pragma unroll 1
+  for (int n = 0; n < 64; ++n)
+    if (ptx::ld_volatile_shared(turn) == v) return true;
+  return wait_turn_slow(turn, v, c);
 }
 
 // Teardown wait: ignores the abort flag, short fixed limit.
@@ -523,6 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto drain = [&](uint32_t e) { return bar0 + 8u * (5 * kMaxStages + 5 + e); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * L::kBarCount);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // ring items whose MMAs have been issued (the two issuers take turns)
+  const uint32_t mma_turn = ptx::smem_u32(tmem_slot + 2);
   const Ctl ctl{abort_flag, p.status, p.timeout_ns};
   // Barriers the leader owns, addressed from either CTA of the pair.
   auto to_leader = [&](uint32_t local_bar) {
@@ -546,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(drain(0), 1);
     ptx::mbar_init(drain(1), 1);
     *abort_flag = 0;
+    ptx::st_volatile_shared(mma_turn, 0u);
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -692,8 +727,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // full barrier in order and signs every item's release, so neither can
     // fall two phases behind on a barrier it tracks by parity.
     // Every MMA accumulates: the epilogue zeroes the accumulator when it has
-    // read it (and once before the first tile), so the order in which the
-    // two issuers' MMAs reach the tensor core does not matter.
+    // read it (and once before the first tile), so no MMA waits for another to
+    // complete.  The issuers still take turns through a shared-memory word
+    // (no tensor-pipe fence, so nothing drains): the MMAs of successive items
+    // enter the tensor core in ring order and the output is bit-reproducible.
     if (lane == 0 && leader) {
       const uint32_t me = warp == 1 ? 0u : 1u;
       int stage = 0;
@@ -734,10 +771,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if ((j & 1u) == me) {
-            ptx::tc_fence_after();
+            // Everything the MMAs need is computed before this issuer's turn.
             const uint32_t st = sbase + stage * L::kStageBytes;
-            if (i < w.lora) {
-              const int nsteps = min(2, (p.r16 - kLoraRanks * i) / 16);
+            const bool lora_item = i < w.lora;
+            int nsteps;  // MMAs of this item
+            if (lora_item) {
+              nsteps = min(2, (p.r16 - kLoraRanks * i) / 16);
+            } else {
+              // K=64 steps present in this item (the last K block may be partial)
+              nsteps = L::kSteps;
+              if (k_ragged) {
+                const int kb0 = KBI * unit_k_item<SK>(p, w, i - w.lora, rot);
+                nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
+              }
+            }
+            const uint32_t sf = tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
+            // descriptors of this stage's first K step; a step advances the
+            // start address (descriptor units of 16 bytes)
+            const uint64_t soff = static_cast<uint64_t>((stage * L::kStageBytes) >> 4);
+            const uint64_t ad0 = desc_a0 + soff, bd0 = desc_b0 + soff;
+            auto step = [&](int ks) {
+              const int kk = ks >> 2, s4 = ks & 3;
+              const uint64_t ad = ad0 + static_cast<uint64_t>((kk * L::kATile + 32 * s4) >> 4);
+              const uint64_t bd = bd0 + static_cast<uint64_t>((kk * L::kBTile + 32 * s4) >> 4);
+              const uint32_t sfa = sf + 4 * ks;
+              const uint32_t sfb = sf + 4 * L::kSteps + 4 * ks * L::kSfbHalves;
+              if (CG == 2)
+                ptx::mma_mxf4nvf4_pair(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
+              else
+                ptx::mma_mxf4nvf4(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
+            };
+            // Items reach the tensor core in ring order: the fp32 accumulation
+            // order, and with it every output bit, is the same on every call
+            // (unless the caller relaxed the order for the last few percent).
+            if (p.ordered && !wait_turn(mma_turn, j, ctl)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            if (lora_item) {
               for (int s = 0; s < nsteps; ++s) {
                 const uint64_t ad = ptx::desc_kmajor_sw64(st + L::kLoraLA + 32 * s);
                 const uint64_t bd = ptx::desc_kmajor_sw64(st + L::kLoraLU + 32 * s);
@@ -746,37 +818,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                   ptx::mma_bf16(d_tmem, ad, bd, kIdescLora, 1u);
               }
-            } else {
-              const uint32_t sf =
-                  tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
-              // descriptors of this stage's first K step; a step advances the
-              // start address (descriptor units of 16 bytes)
-              const uint64_t soff = static_cast<uint64_t>((stage * L::kStageBytes) >> 4);
-              const uint64_t ad0 = desc_a0 + soff, bd0 = desc_b0 + soff;
-              auto step = [&](int ks) {
-                const int kk = ks >> 2, s4 = ks & 3;
-                const uint64_t ad = ad0 + static_cast<uint64_t>((kk * L::kATile + 32 * s4) >> 4);
-                const uint64_t bd = bd0 + static_cast<uint64_t>((kk * L::kBTile + 32 * s4) >> 4);
-                const uint32_t sfa = sf + 4 * ks;
-                const uint32_t sfb = sf + 4 * L::kSteps + 4 * ks * L::kSfbHalves;
-                if (CG == 2)
-                  ptx::mma_mxf4nvf4_pair(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
-                else
-                  ptx::mma_mxf4nvf4(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
-              };
-              // K=64 steps present in this item (the last K block may be partial)
-              int nsteps = L::kSteps;
-              if (k_ragged) {
-                const int kb0 = KBI * unit_k_item<SK>(p, w, i - w.lora, rot);
-                nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
-              }
-              if (nsteps == L::kSteps) {
+            } else if (nsteps == L::kSteps) {
 #pragma unroll
-                for (int ks = 0; ks < L::kSteps; ++ks) step(ks);
-              } else {
-                for (int ks = 0; ks < nsteps; ++ks) step(ks);
-              }
+              for (int ks = 0; ks < L::kSteps; ++ks) step(ks);
+            } else {
+              for (int ks = 0; ks < nsteps; ++ks) step(ks);
             }
+            ptx::st_volatile_shared(mma_turn, j + 1);
             if (CG == 2)
               ptx::mma_commit_pair_multicast(empty(stage), 3);
             else

@@ -93,6 +93,8 @@ def call(lib, M=256, N=256, K=256, R=32, ptrs=None, opts=None, prepacked=False):
     (dict(opts=dict(k_splits=9)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(k_splits=-2)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(act_scales_packed=2)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(relaxed_order=2)), binding.SVDQ_ERR_BAD_OPTION),
+    (dict(opts=dict(relaxed_order=-1)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(io_dtype=2)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(cta_group=3)), binding.SVDQ_ERR_BAD_OPTION),
     (dict(opts=dict(cta_group=2, tile_n=128)), binding.SVDQ_ERR_BAD_OPTION),

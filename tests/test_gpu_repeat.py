@@ -1,0 +1,57 @@
+"""Bit-reproducibility through the C ABI: the same call on the same inputs gives
+the same output bits every time.
+
+Every MMA accumulates in fp32, so the order in which ring items reach the
+tensor core decides the last bits of the result.  By default the two MMA
+issuer threads take turns, so that order is the ring order on every call,
+whatever the timing of the loads: LoRA items built from direct loads (R not a
+multiple of 8), tile starts after an epilogue (every stage of the ring ready
+at once), full-size shapes with several waves of tiles.  With
+svdq_options_t.relaxed_order the issuers run freely: the bits may change from
+call to call, the result stays within the acceptance bound.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import oracle_y, parity, run_gpu
+from nvfp4_w4a4_quantized_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = [dict(cta_group=1, tile_n=128), dict(cta_group=1, tile_n=256),
+           dict(cta_group=2, tile_n=256)]
+CFG_IDS = ["cg1_n128", "cg1_n256", "cg2_n256"]
+REPEATS = 12
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import oracle
+    from nvfp4_w4a4_quantized_gb300 import build
+    build.build()
+    oracle.build()
+
+
+@pytest.mark.parametrize("M,N,K,R", [(400, 528, 1088, 100), (1024, 1536, 3072, 32),
+                                     (512, 768, 2048, 128), (4096, 3072, 3072, 32)])
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+def test_repeated_calls_bit_identical(M, N, K, R, cfg):
+    inp = synth.make_inputs(M, N, K, R, seed=M + N + K + R)
+    first = run_gpu(inp, M, N, K, R, options=cfg)
+    for _ in range(REPEATS - 1):
+        y = run_gpu(inp, M, N, K, R, options=cfg)
+        assert np.array_equal(y, first), \
+            f"{int((y != first).sum())} of {y.size} outputs differ between repeated calls"
+
+
+@pytest.mark.parametrize("M,N,K,R", [(400, 528, 1088, 100), (512, 768, 2048, 128)])
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+def test_relaxed_order_within_bound(M, N, K, R, cfg):
+    inp = synth.make_inputs(M, N, K, R, seed=M + N + K + R + 1)
+    ref = oracle_y(inp, M, N, K, R)
+    for _ in range(4):
+        parity(run_gpu(inp, M, N, K, R, options=dict(cfg, relaxed_order=1)), ref)
