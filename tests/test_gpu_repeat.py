@@ -15,8 +15,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import oracle_y, parity, run_gpu
-from nvfp4_w4a4_quantized_gb300 import synth
+from gpu_util import oracle_y, parity, prepack_gpu, run_gpu, run_gpu_prepacked, run_gpu_split
+from nvfp4_w4a4_quantized_gb300 import binding, synth
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +44,42 @@ def test_repeated_calls_bit_identical(M, N, K, R, cfg):
     first = run_gpu(inp, M, N, K, R, options=cfg)
     for _ in range(REPEATS - 1):
         y = run_gpu(inp, M, N, K, R, options=cfg)
+        assert np.array_equal(y, first), \
+            f"{int((y != first).sum())} of {y.size} outputs differ between repeated calls"
+
+
+def _packed_scales(inp, M, N, K, R, cfg):
+    """Prepacked weights and activation scales in the word layout."""
+    d = prepack_gpu(inp, R)
+    d["ascales"] = binding.svdq_pack_scales(d["ascales"])
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    binding.svdq_w4a4_gemm_prepacked(d["act"], d["wgt"], d["ascales"], d["wscales"],
+                                     d["lora_act_in"], d["lora_up"], d.get("wcscale"),
+                                     d.get("bias"), out, options=dict(cfg, act_scales_packed=1))
+    torch.cuda.synchronize()
+    code, site, _ = binding.svdq_read_device_status(clear=True)
+    assert code == 0, f"device status {code} at wait site {site}"
+    return out.double().cpu().numpy()
+
+
+ROUTES = {
+    "prepacked": lambda inp, M, N, K, R, cfg: run_gpu_prepacked(inp, M, N, K, R, options=cfg),
+    "packed_scales": _packed_scales,
+    "split_k3": lambda inp, M, N, K, R, cfg: run_gpu_split(inp, M, N, K, R,
+                                                           options=dict(cfg, k_splits=3))[0],
+    "fp16": lambda inp, M, N, K, R, cfg: run_gpu(inp, M, N, K, R, options=cfg),
+}
+
+
+@pytest.mark.parametrize("route", list(ROUTES))
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+def test_every_route_bit_identical(route, cfg):
+    # 4096 = 16 K blocks: three K splits of 5-6 blocks; 8 to 32 tiles per config
+    M, N, K, R = 512, 1024, 4096, 64
+    inp = synth.make_inputs(M, N, K, R, seed=11, half=(route == "fp16"))
+    first = ROUTES[route](inp, M, N, K, R, cfg)
+    for _ in range(5):
+        y = ROUTES[route](inp, M, N, K, R, cfg)
         assert np.array_equal(y, first), \
             f"{int((y != first).sum())} of {y.size} outputs differ between repeated calls"
 
