@@ -28,6 +28,9 @@ once before timing) and implies `--prepacked`.
 timing; the planner decides the split, e.g. on mlp_down_256x3072x12288_r128).
 Calls are bit-reproducible by default (the MMA issuers take turns);
 `--relaxed-order` times svdq_options_t.relaxed_order = 1 instead.
+A default run (no route flag) also records, under `routes`, the prepacked,
+prepacked + packed-scale and relaxed-order routes of the same workload, timed
+the same way (flushed L2, per-launch events, 10 launches each).
 """
 
 from __future__ import annotations
@@ -416,6 +419,52 @@ def run_ours(args, w, rank, world, local_rank):
     if code != 0:
         raise RuntimeError(f"device status {code} at wait site {site} in the back-to-back run")
 
+    # secondary: the same workload through the other routes of the same operator
+    # (weights prepacked once, activation scales in the word layout, relaxed
+    # issue order), timed like the primary figure: L2 flushed, one event pair
+    # per launch, mean of 10 after 3 warm-up launches.  Default runs only.
+    routes = None
+    plain = not (args.dense or args.fp16 or args.prepacked or args.split or args.packed_scales
+                 or args.relaxed_order)
+    if plain:
+        routes = {}
+        try:
+            wpk, lup = pkg.svdq_prepack_weights(d["wscales"], d["lora_up"] if w.R else None,
+                                                d.get("wcscale"))
+            apk = pkg.svdq_pack_scales(d["ascales"])
+            torch.cuda.synchronize(dev)
+            cases = {"prepacked": (d["ascales"], {}),
+                     "prepacked_packed_scales": (apk, dict(act_scales_packed=1)),
+                     "prepacked_packed_scales_relaxed_order": (apk, dict(act_scales_packed=1,
+                                                                         relaxed_order=1))}
+            for name, (asc, extra) in cases.items():
+                o2 = dict(opts, **extra)
+
+                def call():
+                    pkg.svdq_w4a4_gemm_prepacked(d["act"], d["wgt"], asc, wpk, d.get("lora_act_in"),
+                                                 lup, d.get("wcscale"), d.get("bias"), out,
+                                                 stream=stream, options=o2)
+                for _ in range(3):
+                    flush.zero_()
+                    call()
+                t = []
+                for _ in range(10):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    call()
+                    e1.record(stream)
+                    torch.cuda.synchronize(dev)
+                    t.append(e0.elapsed_time(e1))
+                r_ms = statistics.mean(t)
+                routes[name] = {"ms_per_launch": r_ms,
+                                "value": job_tflops(float(w.flops), world, r_ms), "unit": "TFLOPS"}
+        except Exception as exc:
+            routes = {"skipped": f"{type(exc).__name__}: {exc}"[:200]}
+        code, site, _ = pkg.svdq_read_device_status(clear=True)
+        if code != 0:
+            raise RuntimeError(f"device status {code} at wait site {site} in the route timings")
+
     # end to end through the public call: pinned host inputs -> device -> op -> host
     host = {k: v.pin_memory() for k, v in host_src.items()}
     host_out = torch.empty((w.M, w.N), dtype=out_dtype).pin_memory()
@@ -478,6 +527,7 @@ def run_ours(args, w, rank, world, local_rank):
             "clocks": clk.summary(),
             "hot_l2": hot,
             "back_to_back_cold": b2b,
+            "routes": routes,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
