@@ -144,6 +144,11 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
+            # nvidia-smi's start-up briefly disturbs the GPU: let it write its
+            # first sample before the timed region begins
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.05)
             time.sleep(0.3)
         except Exception:
             self.proc = None
