@@ -316,7 +316,10 @@ int svdq_read_device_status(int32_t* code, int32_t* site, int32_t* block, int cl
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* svdq_status_string(int status);
 
-/* Library ABI version (major * 10000 + minor * 100 + patch). */
+/* Library ABI version (major * 10000 + minor * 100 + patch).  The structs
+ * above grow only at their end; a caller built against a header with another
+ * major.minor (SVDQ_ABI_VERSION / 100) must not pass them to this library. */
+#define SVDQ_ABI_VERSION 400
 int svdq_version(void);
 
 #ifdef __cplusplus

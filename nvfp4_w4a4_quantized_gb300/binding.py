@@ -14,6 +14,8 @@ from typing import Optional
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsvdq.so")
+# include/svdq.h SVDQ_ABI_VERSION the structs below mirror
+ABI_VERSION = 400
 
 SVDQ_OK = 0
 SVDQ_ERR_INVALID_ARG = -1
@@ -120,6 +122,10 @@ def load(path: Optional[str] = None):
         lib.svdq_status_string.argtypes = [ctypes.c_int]
         lib.svdq_version.restype = ctypes.c_int
         lib.svdq_version.argtypes = []
+        # the ctypes structs here mirror include/svdq.h at ABI_VERSION
+        if lib.svdq_version() // 100 != ABI_VERSION // 100:
+            raise RuntimeError(f"{p} has ABI version {lib.svdq_version()}, this binding "
+                               f"expects {ABI_VERSION}: rebuild the library")
         if path is None:
             _lib = lib
         return lib

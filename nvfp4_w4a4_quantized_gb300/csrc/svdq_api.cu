@@ -841,7 +841,7 @@ extern "C" const char* svdq_status_string(int status) {
   }
 }
 
-extern "C" int svdq_version(void) { return 300; }
+extern "C" int svdq_version(void) { return SVDQ_ABI_VERSION; }
 
 extern "C" int svdq_w4a4_gemm_split_noalloc(const void* act, const void* wgt, const void* ascales,
                                             const void* wscales, const float* lora_act_in,

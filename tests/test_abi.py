@@ -47,7 +47,13 @@ def test_status_strings(lib):
         s = binding.status_string(code)
         assert s.startswith("SVDQ_")
     assert binding.status_string(-99) == "SVDQ_ERR_UNKNOWN"
-    assert binding.svdq_version() >= 200
+    assert binding.svdq_version() == binding.ABI_VERSION
+
+
+def test_abi_version_matches_header(lib):
+    import re
+    src = open(os.path.join(os.path.dirname(__file__), "..", "include", "svdq.h")).read()
+    assert int(re.search(r"#define SVDQ_ABI_VERSION (\d+)", src).group(1)) == binding.ABI_VERSION
 
 
 # ---------------------------------------------------------------- validation
