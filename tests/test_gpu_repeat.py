@@ -91,3 +91,13 @@ def test_relaxed_order_within_bound(M, N, K, R, cfg):
     ref = oracle_y(inp, M, N, K, R)
     for _ in range(4):
         parity(run_gpu(inp, M, N, K, R, options=dict(cfg, relaxed_order=1)), ref)
+
+
+@pytest.mark.parametrize("route", ["prepacked", "packed_scales", "split_k3"])
+@pytest.mark.parametrize("cfg", CONFIGS, ids=CFG_IDS)
+def test_relaxed_order_routes_within_bound(route, cfg):
+    M, N, K, R = 512, 1024, 4096, 64
+    inp = synth.make_inputs(M, N, K, R, seed=13)
+    ref = oracle_y(inp, M, N, K, R)
+    for _ in range(2):
+        parity(ROUTES[route](inp, M, N, K, R, dict(cfg, relaxed_order=1)), ref)
