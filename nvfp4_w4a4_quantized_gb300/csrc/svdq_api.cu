@@ -237,6 +237,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* 
   if (rc != SVDQ_OK) return rc;
   pl.num_units = pl.num_tiles * pl.splits;
   if (clusters > pl.num_units) clusters = pl.num_units;
+  // Balanced persistent grid: keep the number of rounds (units per cluster on
+  // the busiest cluster) and use the fewest clusters that need no more, so every
+  // cluster gets the same number of units, give or take one (192 tiles on 76
+  // pairs: 3 rounds -> 64 pairs).  Less contention for the same critical path.
+  if (clusters > 0) {
+    const long long rounds = (pl.num_units + clusters - 1) / clusters;
+    clusters = (pl.num_units + rounds - 1) / rounds;
+  }
   pl.grid = static_cast<int>(clusters * pl.cta_group);
   if (pl.splits > 1) {
     // fp32 partial tiles of the non-final splits (one slot per tile, split,

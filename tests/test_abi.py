@@ -185,7 +185,10 @@ def test_plan_budgets(lib, w):
     assert plan["num_ab_stage"] >= 2
     tiles = -(-w.M // plan["tile_m"]) * -(-w.N // plan["tile_n"])
     assert plan["num_tiles"] == tiles
-    assert plan["grid"] == cg * min(tiles, SMS // cg)
+    # balanced persistent grid: the rounds of the full grid on the fewest clusters
+    rounds = -(-tiles // (SMS // cg))
+    assert plan["grid"] == cg * -(-tiles // rounds)
+    assert plan["grid"] <= SMS
 
 
 @pytest.mark.parametrize("cg,tn", [(1, 128), (1, 256), (2, 256)])
