@@ -144,8 +144,8 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
-            # nvidia-smi's start-up briefly disturbs the GPU: let it write its
-            # first sample before the timed region begins
+            # wait for the first sample, so that sampling covers the warm-up
+            # and timed steps that follow
             t0 = time.time()
             while time.time() - t0 < 3.0 and os.path.getsize(self.path) == 0:
                 time.sleep(0.05)
@@ -337,17 +337,18 @@ def run_ours(args, w, rank, world, local_rank):
              dd.get("lora_up"), dd.get("wcscale"), dd.get("bias"), o, stream=stream, options=opts)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-    code, site, _ = pkg.svdq_read_device_status(clear=True)
-    if code != 0:
-        raise RuntimeError(f"device status {code} at wait site {site} during warm-up")
-
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
+        # warm-up right before the timed steps: an idle GPU lowers its clock,
+        # and the sampler's start-up leaves it idle for a moment
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize(dev)
+        code, site, _ = pkg.svdq_read_device_status(clear=True)
+        if code != 0:
+            raise RuntimeError(f"device status {code} at wait site {site} during warm-up")
         barrier()
         torch.cuda.synchronize(dev)
         t_wall0 = time.perf_counter()
