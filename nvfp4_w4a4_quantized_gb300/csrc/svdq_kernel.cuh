@@ -37,9 +37,11 @@
 //                swizzle).  LoRA ring item (32 ranks): raw fp32 LA rows, 16-bit
 //                LU rows (64-byte swizzle) and wcscale.
 //   warps 1, 14  MMA issuers (one thread each, leader CTA), alternating ring
-//                items: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X for
-//                main items, kind::f16 (bf16 or fp16) for LoRA items, commits
-//                that free ring stages / publish accumulators.
+//                items and taking turns (a shared-memory turn word keeps the
+//                items in ring order): tcgen05.mma kind::mxf4nvf4
+//                block_scale.scale_vec::4X for main items, kind::f16 (bf16 or
+//                fp16) for LoRA items, commits that free ring stages / publish
+//                accumulators.
 //   warps 2, 3   LoRA operand builders: LU' = round16(LU / wc), half the rows
 //                each, in place in the stage's K-major 64-byte-swizzle layout
 //                (nothing to do for prepacked weights, whose LU' arrives ready).
