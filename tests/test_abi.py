@@ -289,3 +289,16 @@ def test_split_plan_forced_and_rejected(lib):
 ])
 def test_pack_scales_host_validation(lib, args, expect):
     assert lib.svdq_pack_scales(*args, None) == expect
+
+
+@pytest.mark.parametrize("M,N", [(256, 256), (1024, 3072), (4096, 3072), (4096, 12288),
+                                 (16384, 12288), (2816, 2816), (4352, 3840)])
+def test_plan_balanced_grid(lib, M, N):
+    # the full grid's number of rounds, on the fewest clusters that keep it
+    plan = binding.svdq_query_plan(M, N, 3072, 32, options=dict(cta_group=2), sm_count=SMS)
+    units, cg = plan["num_units"], plan["cta_group"]
+    clusters = plan["grid"] // cg
+    full = min(units, SMS // cg)
+    rounds = -(-units // full)
+    assert -(-units // clusters) == rounds
+    assert clusters == 1 or -(-units // (clusters - 1)) > rounds
