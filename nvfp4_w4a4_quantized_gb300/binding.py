@@ -16,6 +16,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsvdq.so")
 # include/svdq.h SVDQ_ABI_VERSION the structs below mirror
 ABI_VERSION = 400
+# include/svdq.h size limits
+SVDQ_MAX_MN = 1 << 24
+SVDQ_MAX_K = 1 << 20
+SVDQ_MAX_RANK = 128
 
 SVDQ_OK = 0
 SVDQ_ERR_INVALID_ARG = -1

@@ -54,6 +54,9 @@ def test_abi_version_matches_header(lib):
     import re
     src = open(os.path.join(os.path.dirname(__file__), "..", "include", "svdq.h")).read()
     assert int(re.search(r"#define SVDQ_ABI_VERSION (\d+)", src).group(1)) == binding.ABI_VERSION
+    assert "#define SVDQ_MAX_MN (1LL << 24)" in src and binding.SVDQ_MAX_MN == 1 << 24
+    assert "#define SVDQ_MAX_K (1LL << 20)" in src and binding.SVDQ_MAX_K == 1 << 20
+    assert "#define SVDQ_MAX_RANK 128" in src and binding.SVDQ_MAX_RANK == 128
 
 
 # ---------------------------------------------------------------- validation
