@@ -31,7 +31,14 @@ Calls are bit-reproducible by default (the MMA issuers take turns);
 `--relaxed-order` times svdq_options_t.relaxed_order = 1 instead.
 A default run (no route flag) also records, under `routes`, the prepacked,
 prepacked + packed-scale and relaxed-order routes of the same workload, timed
-the same way (flushed L2, per-launch events, 10 launches each).
+the same way (flushed L2, per-launch events, 10 launches each), and under
+`per_shape` every benchmark workload timed the same way: the tiny case, the
+attention projection, MLP-up and MLP-down, each on the default route, the
+dense calibration variant (R = 0, no wcscale / bias) and the prepacked +
+packed-scale route, and the 24-case token-count sweep (default route, plus
+the split-K entry point where the planner splits).  The headline `value` is
+the attention projection, the configuration the metric is quoted on.
+`--no-per-shape` skips that section.
 """
 
 from __future__ import annotations
@@ -78,6 +85,8 @@ def parse():
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-per-shape", action="store_true",
+                    help="skip the per-shape section of a default run")
     return ap.parse_args()
 
 
@@ -278,6 +287,113 @@ def run_reference(args, w, rank):
         "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def time_flushed(call, flush, stream, n_warm, n_timed, torch, dev):
+    """Per-launch CUDA-event times (ms) of `call`, with the L2 flushed by a
+    memset outside each event pair."""
+    for _ in range(n_warm):
+        flush.zero_()
+        call()
+    t = []
+    for _ in range(n_timed):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t.append(e0.elapsed_time(e1))
+    return t
+
+
+def shape_entry(flops, ms, fp4_peak, plan=None):
+    mean = statistics.mean(ms)
+    tf = flops / (mean * 1e-3) / 1e12
+    e = {"ms_mean": mean, "ms_median": statistics.median(ms), "ms_min": min(ms),
+         "launches": len(ms), "tflops": tf, "mfu_vs_10pf": tf / BASELINE_PEAK_TFLOPS,
+         "frac": tf / fp4_peak}
+    if plan is not None:
+        e["plan"] = {"tile": [plan["tile_m"], plan["tile_n"]], "stages": plan["num_ab_stage"],
+                     "grid": plan["grid"], "k_splits": plan["k_splits"]}
+    return e
+
+
+def run_per_shape(pkg, synth, torch, dev, stream, flush, fp4_peak):
+    """Every benchmark workload on one GPU, timed like the headline figure
+    (L2 flushed before each launch, one event pair per launch)."""
+    res = {}
+    prod = [synth.TINY, synth.ATTN_PROJ, synth.MLP_UP, synth.MLP_DOWN]
+    for w in prod:
+        inp = synth.make_workload_inputs(w)
+        d = {k: v.to(dev) for k, v in inp.items()}
+        out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        plan = pkg.svdq_query_plan(w.M, w.N, w.K, w.R)
+
+        def call(dd=d, r=w.R, wc=True):
+            pkg.svdq_w4a4_gemm(dd["act"], dd["wgt"], dd["ascales"], dd["wscales"],
+                               dd["lora_act_in"] if r else None, dd["lora_up"] if r else None,
+                               dd["wcscale"] if wc else None, dd["bias"] if wc else None, out,
+                               stream=stream)
+        e = shape_entry(float(w.flops), time_flushed(call, flush, stream, 3, 10, torch, dev),
+                        fp4_peak, plan)
+        e.update({"M": w.M, "N": w.N, "K": w.K, "R": w.R})
+        # dense calibration: the same shape and kernel, R = 0, no wcscale / bias
+        dense_flops = 2.0 * w.M * w.N * w.K
+        e["dense"] = shape_entry(dense_flops, time_flushed(lambda: call(r=0, wc=False), flush,
+                                                           stream, 3, 10, torch, dev), fp4_peak)
+        # weights prepacked once, activation scales in the word layout
+        wpk, lup = pkg.svdq_prepack_weights(d["wscales"], d["lora_up"], d["wcscale"])
+        apk = pkg.svdq_pack_scales(d["ascales"])
+        torch.cuda.synchronize(dev)
+        o2 = dict(act_scales_packed=1)
+
+        def call_pk():
+            pkg.svdq_w4a4_gemm_prepacked(d["act"], d["wgt"], apk, wpk, d["lora_act_in"], lup,
+                                         d["wcscale"], d["bias"], out, stream=stream, options=o2)
+        e["prepacked_packed_scales"] = shape_entry(
+            float(w.flops), time_flushed(call_pk, flush, stream, 3, 10, torch, dev), fp4_peak)
+        res[w.name] = e
+        del d, out, wpk, lup, apk
+    sweep = []
+    for w in synth.sweep_workloads():
+        inp = synth.make_workload_inputs(w)
+        d = {k: v.to(dev) for k, v in inp.items()}
+        out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        plan = pkg.svdq_query_plan(w.M, w.N, w.K, w.R)
+
+        def call(dd=d):
+            pkg.svdq_w4a4_gemm(dd["act"], dd["wgt"], dd["ascales"], dd["wscales"],
+                               dd["lora_act_in"], dd["lora_up"], dd["wcscale"], dd["bias"], out,
+                               stream=stream)
+        e = shape_entry(float(w.flops), time_flushed(call, flush, stream, 2, 5, torch, dev),
+                        fp4_peak, plan)
+        e.update({"name": w.name, "M": w.M, "N": w.N, "K": w.K, "R": w.R})
+        wsz = pkg.svdq_workspace_size(w.M, w.N, w.K, w.R, options=dict(k_splits=-1))
+        if wsz > 0:
+            ws = torch.zeros(wsz, dtype=torch.uint8, device=dev)
+            splan = pkg.svdq_query_plan(w.M, w.N, w.K, w.R, options=dict(k_splits=-1))
+
+            def call_split(dd=d):
+                pkg.svdq_w4a4_gemm_split(dd["act"], dd["wgt"], dd["ascales"], dd["wscales"],
+                                         dd["lora_act_in"], dd["lora_up"], dd["wcscale"],
+                                         dd["bias"], out, ws, stream=stream,
+                                         options=dict(k_splits=-1))
+            e["split"] = shape_entry(float(w.flops), time_flushed(call_split, flush, stream, 2, 5,
+                                                                  torch, dev), fp4_peak, splan)
+            del ws
+        sweep.append(e)
+        del d, out
+    tfs = sorted(max(s["tflops"], s.get("split", {}).get("tflops", 0.0)) for s in sweep)
+    res["sweep"] = {"cases": sweep, "tflops_min": tfs[0], "tflops_median": statistics.median(tfs),
+                    "tflops_max": tfs[-1],
+                    "how": "svdq_w4a4_gemm per case (and svdq_w4a4_gemm_split where the planner "
+                           "splits; the summary takes the faster), 2 warm-up + 5 timed flushed "
+                           "launches"}
+    code, site, _ = pkg.svdq_read_device_status(clear=True)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at wait site {site} in the per-shape runs")
+    return res
 
 
 def run_ours(args, w, rank, world, local_rank):
@@ -544,6 +660,16 @@ def run_ours(args, w, rank, world, local_rank):
     fp4_peak = bf16_peak * NOMINAL_FP4_OVER_BF16
     traffic = committed_traffic(w.name)
 
+    per_shape = None
+    if plain and rank == 0 and not args.no_per_shape:
+        with ClockSampler(local_rank) as clk2:
+            try:
+                per_shape = run_per_shape(pkg, synth, torch, dev, stream, flush, fp4_peak)
+            except Exception as exc:
+                per_shape = {"skipped": f"{type(exc).__name__}: {exc}"[:300]}
+        if isinstance(per_shape, dict):
+            per_shape["clocks"] = clk2.summary()
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, rows, secs, threads = oracle_sample(w, inp, target_s=12.0)
@@ -584,6 +710,7 @@ def run_ours(args, w, rank, world, local_rank):
             "hot_l2": hot,
             "back_to_back_cold": b2b,
             "routes": routes,
+            "per_shape": per_shape,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -40,6 +40,14 @@ extern "C" {
                                           svdq_workspace_size, or not 256-byte aligned  */
 #define SVDQ_ERR_SCRATCH_LIMIT -10     /* the plan needs more scratch than the library's
                                           fixed SVDQ_NOALLOC_SCRATCH_BYTES              */
+#define SVDQ_ERR_WCSCALE_ZERO -11      /* device status only: R > 0 and wcscale[n] == 0 for
+                                          a column n (reported as the status site): the
+                                          LoRA term of that column was dropped, the rest
+                                          of out is computed                            */
+#define SVDQ_ERR_LU_OVERFLOW -12       /* device status only: lora_up[n][r] / wcscale[n]
+                                          is beyond the 16-bit I/O type's range for a
+                                          column n (the site): that column's LoRA term is
+                                          infinite, the rest of out is computed         */
 
 /* Size of the library's own scratch array (svdq_w4a4_gemm_split_noalloc). */
 #define SVDQ_NOALLOC_SCRATCH_BYTES (16LL << 20)
@@ -68,9 +76,15 @@ extern "C" {
  * lora_act_in device, fp32 [M, R] row-major; NULL if and only if R == 0.
  * lora_up     device, bf16 [N, R] row-major; NULL if and only if R == 0.
  * wcscale     device, bf16 [N]; NULL means 1.  With R > 0 every wcscale[n]
- *             must be finite and non-zero (the LoRA operand is pre-divided
- *             by it so that LoRA and the main product share one accumulator);
- *             a zero wcscale[n] drops the LoRA term of column n.
+ *             must be finite and non-zero, and lora_up[n][r] / wcscale[n]
+ *             must fit the 16-bit type: the LoRA operand is pre-divided by
+ *             wcscale so that LoRA and the main product share one
+ *             accumulator.  A column that breaks this gets a wrong LoRA term
+ *             (none for a zero wcscale[n], an infinite one on overflow; in
+ *             fp16 that is |lora_up / wcscale| > 65504) and the launch records
+ *             SVDQ_ERR_WCSCALE_ZERO or SVDQ_ERR_LU_OVERFLOW with the column in
+ *             the device status word (svdq_read_device_status); every other
+ *             column is unaffected.
  * bias        device, bf16 [N]; NULL means 0.
  * out         device, bf16 [M, N] row-major; every element is written.
  * M, N        multiples of 16 (the scale tensors' rows must be 16-byte
@@ -213,13 +227,26 @@ int svdq_w4a4_gemm_prepacked(const void* act, const void* wgt, const void* ascal
  * weights_prepacked == 1), plus:
  * workspace        device, at least svdq_workspace_size(...) bytes, 256-byte
  *                  aligned, zero-filled before its first use; owned by the
- *                  caller and reused across calls.  Calls that share a
- *                  workspace must not overlap on the GPU (they would race on
- *                  its contents).
+ *                  caller and reused across calls.  Every completed call
+ *                  leaves its flags at zero again (a part raises its flag when
+ *                  its partial is stored, the last part lowers it once it has
+ *                  added the partial), so the same workspace serves any later
+ *                  call, including launches replayed from a CUDA graph.  After
+ *                  a launch that recorded SVDQ_ERR_TIMEOUT the flags may be
+ *                  left raised: zero the workspace again before reusing it.
+ *                  Calls that share a workspace must not overlap on the GPU
+ *                  (they would race on its contents).
  * workspace_bytes  its size.
  * When the plan has no split the workspace is not touched.  The summation
  * order of the K parts differs from the unsplit kernel (fp32 partials), so
  * results agree with it within the operator's tolerance, not bit for bit.
+ * The last part of a tile waits (bounded) for the other parts, which the
+ * planner places on clusters of their own so that all parts of a launch are
+ * resident at once.  That holds while the launch has the GPU's SMs to itself:
+ * a split launch running concurrently with other kernels that occupy many
+ * SMs (another stream) may not get all of its parts scheduled in time and
+ * then ends with SVDQ_ERR_TIMEOUT in the device status word instead of a
+ * result.  Run split launches alone on the device, or stream-ordered.
  * Returns SVDQ_ERR_WORKSPACE if the workspace is missing or too small.
  */
 int svdq_w4a4_gemm_split(const void* act, const void* wgt, const void* ascales,
@@ -246,8 +273,11 @@ int svdq_w4a4_gemm_split(const void* act, const void* wgt, const void* ascales,
  * device looks up the array's device address (a one-time set-up per device);
  * make that first call before any stream capture.  Every call on a device
  * shares the one array: calls that overlap on the GPU (other streams, other
- * threads) race on it and must be serialised by the caller.  Flags carry a
- * per-call value, so nothing needs clearing between calls.
+ * threads) race on it and must be serialised by the caller.  The array
+ * starts zero-filled and every completed call leaves its flags at zero, so
+ * nothing needs clearing between calls; after a launch that recorded
+ * SVDQ_ERR_TIMEOUT, svdq_read_device_status with clear != 0 zero-fills the
+ * array again (synchronously) along with the status word.
  */
 int svdq_w4a4_gemm_split_noalloc(const void* act, const void* wgt, const void* ascales,
                                  const void* wscales, const float* lora_act_in,
@@ -308,9 +338,14 @@ int64_t svdq_lora_stage_bytes(int64_t tile_m, int64_t tile_n, int64_t R, int64_t
                               int64_t cta_group, int64_t* la_bytes, int64_t* lu_bytes);
 
 /* Read (and if clear != 0, reset) the library's device status word for the
- * current device: *code is SVDQ_OK or SVDQ_ERR_TIMEOUT, *site identifies
- * the wait that expired, *block the CTA.  Synchronises the device.  Any of
- * the output pointers may be NULL. */
+ * current device.  *code is SVDQ_OK, SVDQ_ERR_TIMEOUT (*site identifies the
+ * wait that expired), SVDQ_ERR_WCSCALE_ZERO or SVDQ_ERR_LU_OVERFLOW (*site is
+ * the column); *block is the CTA that recorded it.  The first condition
+ * recorded since the last reset is kept.  Clearing a SVDQ_ERR_TIMEOUT also
+ * zero-fills the scratch array of svdq_w4a4_gemm_split_noalloc, if that entry
+ * point has been used on this device (a timed-out split launch can leave its
+ * flags raised).  Synchronises the device.  Any of the output pointers may
+ * be NULL. */
 int svdq_read_device_status(int32_t* code, int32_t* site, int32_t* block, int clear);
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -319,7 +354,7 @@ const char* svdq_status_string(int status);
 /* Library ABI version (major * 10000 + minor * 100 + patch).  The structs
  * above grow only at their end; a caller built against a header with another
  * major.minor (SVDQ_ABI_VERSION / 100) must not pass them to this library. */
-#define SVDQ_ABI_VERSION 400
+#define SVDQ_ABI_VERSION 500
 int svdq_version(void);
 
 #ifdef __cplusplus

@@ -15,7 +15,7 @@ from typing import Optional
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsvdq.so")
 # include/svdq.h SVDQ_ABI_VERSION the structs below mirror
-ABI_VERSION = 400
+ABI_VERSION = 500
 # include/svdq.h size limits
 SVDQ_MAX_MN = 1 << 24
 SVDQ_MAX_K = 1 << 20
@@ -32,6 +32,8 @@ SVDQ_ERR_TIMEOUT = -7
 SVDQ_ERR_BAD_OPTION = -8
 SVDQ_ERR_WORKSPACE = -9
 SVDQ_ERR_SCRATCH_LIMIT = -10
+SVDQ_ERR_WCSCALE_ZERO = -11
+SVDQ_ERR_LU_OVERFLOW = -12
 SVDQ_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 SVDQ_IO_BF16 = 0

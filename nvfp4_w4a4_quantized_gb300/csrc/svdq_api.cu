@@ -7,10 +7,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
-#include <atomic>
 #include <cstdint>
 #include <cstring>
-#include <ctime>
 #include <mutex>
 
 #include "svdq.h"
@@ -535,15 +533,6 @@ int device_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t
   return pl->splits > 1 ? ensure_any(cg, bn, f16, true, dinfo) : SVDQ_OK;
 }
 
-// Flag value of a split launch: per-process counter from a time-derived
-// start, never 0 (a zero-filled workspace holds no live flag).
-std::atomic<uint32_t> g_epoch{static_cast<uint32_t>(std::time(nullptr)) * 2654435761u};
-uint32_t next_epoch() {
-  uint32_t e = g_epoch.fetch_add(1) + 1;
-  if (e == 0) e = g_epoch.fetch_add(1) + 1;
-  return e;
-}
-
 int64_t ws_flag_offset(const Plan& pl) {
   return (pl.ws_partial_bytes + kWsAlign - 1) / kWsAlign * kWsAlign;
 }
@@ -601,7 +590,6 @@ int run_gemm(const void* act, const void* wgt, const void* ascales, const void* 
     kp.partials = static_cast<float4*>(workspace);
     kp.flags =
         reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + ws_flag_offset(pl));
-    kp.epoch = next_epoch();
   }
   kp.debug_fault = options ? options->debug_fault : 0;
   kp.ordered = (options != nullptr && options->relaxed_order) ? 0 : 1;
@@ -700,7 +688,7 @@ extern "C" int svdq_pack_scales(const void* scales, int64_t rows, int64_t K, voi
   svdq_prepack_kernel<false><<<static_cast<unsigned>(blocks), 256, 0,
                                static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint8_t*>(scales), nullptr, nullptr, static_cast<uint32_t*>(packed),
-      nullptr, static_cast<int>(rows), static_cast<int>(K), 0);
+      nullptr, static_cast<int>(rows), static_cast<int>(K), 0, dinfo->status);
   if (cudaGetLastError() != cudaSuccess) return SVDQ_ERR_LAUNCH;
   return SVDQ_OK;
 }
@@ -735,11 +723,11 @@ extern "C" int svdq_prepack_weights(const void* wscales, const void* lora_up,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n = static_cast<int>(N), k = static_cast<int>(K), r = static_cast<int>(R);
   if (io_dtype == SVDQ_IO_FP16)
-    svdq_prepack_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(ws, lu, wc, wpk, lup,
-                                                                             n, k, r);
+    svdq_prepack_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        ws, lu, wc, wpk, lup, n, k, r, dinfo->status);
   else
-    svdq_prepack_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(ws, lu, wc, wpk,
-                                                                              lup, n, k, r);
+    svdq_prepack_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        ws, lu, wc, wpk, lup, n, k, r, dinfo->status);
   if (cudaGetLastError() != cudaSuccess) return SVDQ_ERR_LAUNCH;
   return SVDQ_OK;
 }
@@ -828,6 +816,19 @@ extern "C" int svdq_read_device_status(int32_t* code, int32_t* site, int32_t* bl
       cudaGetLastError();
       return SVDQ_ERR_CUDA;
     }
+    // a timed-out split launch may have left flags raised in the library's
+    // scratch: start it from zero again
+    void* scratch = nullptr;
+    {
+      std::lock_guard<std::mutex> lock(g_mutex);
+      scratch = d->noalloc_scratch;
+    }
+    if (st[0] == SVDQ_ERR_TIMEOUT && scratch != nullptr &&
+        (cudaMemset(scratch, 0, SVDQ_NOALLOC_SCRATCH_BYTES) != cudaSuccess ||
+         cudaDeviceSynchronize() != cudaSuccess)) {
+      cudaGetLastError();
+      return SVDQ_ERR_CUDA;
+    }
   }
   return SVDQ_OK;
 }
@@ -845,6 +846,8 @@ extern "C" const char* svdq_status_string(int status) {
     case SVDQ_ERR_BAD_OPTION: return "SVDQ_ERR_BAD_OPTION";
     case SVDQ_ERR_WORKSPACE: return "SVDQ_ERR_WORKSPACE";
     case SVDQ_ERR_SCRATCH_LIMIT: return "SVDQ_ERR_SCRATCH_LIMIT";
+    case SVDQ_ERR_WCSCALE_ZERO: return "SVDQ_ERR_WCSCALE_ZERO";
+    case SVDQ_ERR_LU_OVERFLOW: return "SVDQ_ERR_LU_OVERFLOW";
     default: return "SVDQ_ERR_UNKNOWN";
   }
 }

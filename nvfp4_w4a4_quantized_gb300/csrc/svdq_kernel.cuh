@@ -111,7 +111,9 @@ enum WaitSite : int {
   kSiteSplitFlag = 10,
 };
 
-constexpr int kStatusTimeout = -7;  // == SVDQ_ERR_TIMEOUT
+constexpr int kStatusTimeout = -7;       // == SVDQ_ERR_TIMEOUT
+constexpr int kStatusWcscaleZero = -11;  // == SVDQ_ERR_WCSCALE_ZERO
+constexpr int kStatusLuOverflow = -12;   // == SVDQ_ERR_LU_OVERFLOW
 
 // CG: CTAs per MMA; BN: tile columns; KBI: K blocks (of 256) per main ring
 // item.  Larger items halve the fixed per-item costs (one TMA batch, one
@@ -152,7 +154,7 @@ struct Layout {
   static constexpr int kEpiStageBytes = 32 * 64;
   static constexpr int kEpiBytes = 8 * kEpiStageBytes;
   static constexpr int kWcbBytes = 8 * BN * 4;
-  static constexpr int kBarCount = 5 * kMaxStages + 7;
+  static constexpr int kBarCount = 5 * kMaxStages + 9;
   static constexpr int kBarBytes = 8 * kBarCount + 16;
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   __host__ __device__ static constexpr int epi_offset(int stages) { return stages * kStageBytes; }
@@ -183,9 +185,9 @@ struct KParams {
   int act_packed;   // activation scales arrive as words [K/64][M]
   int splits;       // K splits per tile (1: every unit is a whole tile)
   int num_units;    // num_tiles * splits
-  unsigned int epoch;     // split-K: the value this launch's flags are raised to
   float4* partials;       // split-K: fp32 partial tiles of the non-final splits
-  unsigned int* flags;    // split-K: one per (tile, non-final split, CTA, epilogue warp)
+  unsigned int* flags;    // split-K: one per (tile, non-final split, CTA, epilogue warp);
+                          // 0 between launches, 1 while a partial waits to be added
   int debug_fault;
   int ordered;  // the MMA issuers take turns: bit-reproducible accumulation order
   unsigned long long timeout_ns;
@@ -266,6 +268,26 @@ __device__ __noinline__ void report_timeout(int* status, int site) {
   }
 }
 
+// A LoRA operand the shared accumulator cannot carry: wcscale[n] == 0 with
+// R > 0 (LU' = LU / wcscale does not exist, so column n's LoRA term is
+// dropped) or LU / wcscale[n] beyond the 16-bit type's range (infinite LU').
+// The launch still completes; the first condition recorded in the status
+// word wins, with the column.  Warp-collective: `bad` and `n` per lane.
+__device__ __noinline__ void report_lora_operand(int* status, int code, int n) {
+  if (atomicCAS(status, 0, code) == 0) {
+    status[1] = n;
+    status[2] = static_cast<int>(blockIdx.x);
+  }
+}
+__device__ __forceinline__ void warp_report_lora(int* status, int code, bool bad, int n) {
+  const uint32_t m = __ballot_sync(0xffffffffu, bad);
+  if (m != 0u) {
+    const int src = __ffs(static_cast<int>(m)) - 1;
+    const int col = __shfl_sync(0xffffffffu, n, src);
+    if ((threadIdx.x & 31) == 0) report_lora_operand(status, code, col);
+  }
+}
+
 // Bounded wait for the phase with parity `parity` of a local mbarrier.
 // Returns false (and makes every other role of this CTA give up) on expiry or
 // if another role already gave up.  CLUSTER selects a cluster-scope acquire,
@@ -296,13 +318,17 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, int
   return __all_sync(0xffffffffu, ok);
 }
 
-// Split-K: bounded wait until another split's flag holds this launch's epoch.
-__device__ __forceinline__ bool wait_flag(const unsigned int* f, unsigned int v, const Ctl& c) {
-  if (ptx::ld_acquire_gpu(f) == v) return true;
+// Split-K: bounded wait until another split has raised its flag (non-zero).
+// The waiting split lowers the flag again once it has added the partial, so
+// every completed launch leaves its flags at 0: nothing launch-specific is
+// compared, and a launch replayed from a CUDA graph waits exactly as a fresh
+// one does.
+__device__ __forceinline__ bool wait_flag(const unsigned int* f, const Ctl& c) {
+  if (ptx::ld_acquire_gpu(f) != 0u) return true;
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
     __nanosleep(64);
-    if (ptx::ld_acquire_gpu(f) == v) return true;
+    if (ptx::ld_acquire_gpu(f) != 0u) return true;
     if (*c.abort_flag) return false;
     if (ptx::globaltimer() - t0 > c.timeout_ns) {
       *c.abort_flag = 1;
@@ -310,35 +336,6 @@ __device__ __forceinline__ bool wait_flag(const unsigned int* f, unsigned int v,
       return false;
     }
   }
-}
-
-// Bounded wait until the turn word (a shared-memory address) reaches v: the
-// other MMA issuer has issued the MMAs of item v - 1.  The slow path of
-// wait_turn, kept out of line: code inlined into the issuers' loop slows
-// every ring item, even where it never runs.  The abort flag and the time
-// limit are checked every 64 polls.
-__device__ __noinline__ bool wait_turn_slow(uint32_t turn, uint32_t v, const Ctl& c) {
-  const uint64_t t0 = ptx::globaltimer();
-  while (true) {
-#pragma unroll 1
-    for (int n = 0; n < 64; ++n)
-      if (ptx::ld_volatile_shared(turn) == v) return true;
-    if (*c.abort_flag) return false;
-    if (ptx::globaltimer() - t0 > c.timeout_ns) {
-      *c.abort_flag = 1;
-      report_timeout(c.status, kSiteMmaTurn);
-      return false;
-    }
-  }
-}
-
-// The usual hand-off takes a few polls: spin briefly inline, then fall back
-// to the bounded wait.
-__device__ __forceinline__ bool wait_turn(uint32_t turn, uint32_t v, const Ctl& c) {
-#pragma unroll 1
-  for (int n = 0; n < 64; ++n)
-    if (ptx::ld_volatile_shared(turn) == v) return true;
-  return wait_turn_slow(turn, v, c);
 }
 
 // Teardown wait: ignores the abort flag, short fixed limit.
@@ -362,6 +359,7 @@ struct H16 {
   static __device__ __forceinline__ float hi(uint32_t w) { return bf16_hi(w); }
   static __device__ __forceinline__ uint32_t pack(float a, float b) { return ptx::pack_bf16x2(a, b); }
   static constexpr uint32_t kOnes = 0x3F803F80u;  // (1.0, 1.0)
+  static constexpr uint32_t kInf = 0x7F80u;       // exponent all ones, mantissa 0
 };
 template <>
 struct H16<true> {
@@ -372,7 +370,14 @@ struct H16<true> {
   static __device__ __forceinline__ float hi(uint32_t w) { return one(uint16_t(w >> 16)); }
   static __device__ __forceinline__ uint32_t pack(float a, float b) { return ptx::pack_f16x2(a, b); }
   static constexpr uint32_t kOnes = 0x3C003C00u;
+  static constexpr uint32_t kInf = 0x7C00u;
 };
+
+// Either 16-bit half of a packed pair is +-infinity.
+template <bool F16>
+__device__ __forceinline__ bool has_inf16(uint32_t w) {
+  return ((w & 0x7FFFu) == H16<F16>::kInf) || (((w >> 16) & 0x7FFFu) == H16<F16>::kInf);
+}
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
@@ -405,6 +410,17 @@ __device__ __forceinline__ void sf_words(const uint8_t* raw, int pitch, int lane
   w[3] = __byte_perm(t1, t3, 0x7632);
 }
 
+// One 32-column group of packed 16-bit outputs (v[2k], v[2k+1] = columns
+// 4k .. 4k+3) as row `lane` of a 32 x 32 staging tile with 64-byte rows and
+// the 64-byte swizzle: 16-byte chunk j holds columns 8j .. 8j+7 at chunk
+// index j XOR bits 1..2 of the row.
+__device__ __forceinline__ void stage_row(uint8_t* stg, int lane, const uint32_t* v) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(stg + 64 * lane + ((j ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..3) of row `row` in a K-major tile
 // with 64-byte rows and the 64-byte swizzle.
 __device__ __forceinline__ int sw64_offset(int row, int chunk) {
@@ -430,16 +446,25 @@ __device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* r
 }
 
 // 1/wcscale for tile rows r0 + lane + 32t (t < NR/32), 0 outside N or for a
-// zero wcscale (fp32 reciprocal, correctly rounded).
+// zero wcscale (fp32 reciprocal, correctly rounded; a zero inside N is
+// reported in the status word).
 template <int NR, bool F16>
 __device__ __forceinline__ void lora_inv_wc(float* inv, const uint8_t* wc, int n_cta, int N,
-                                            int r0, int lane) {
+                                            int r0, int lane, int* status) {
+  bool zero = false;
+  int zn = 0;
 #pragma unroll
   for (int t = 0; t < NR / 32; ++t) {
     const int off = quad_row(r0 + lane + 32 * t);
     const float w = H16<F16>::one(*reinterpret_cast<const uint16_t*>(wc + 2 * off));
-    inv[t] = (n_cta + off < N && w != 0.f) ? __frcp_rn(w) : 0.f;
+    const bool in = n_cta + off < N;
+    inv[t] = (in && w != 0.f) ? __frcp_rn(w) : 0.f;
+    if (in && w == 0.f) {
+      zero = true;
+      zn = n_cta + off;
+    }
   }
+  warp_report_lora(status, kStatusWcscaleZero, zero, zn);
 }
 
 // LU' rows r0 .. r0+NR-1 in place: every 16-byte chunk of tile row r (column
@@ -449,11 +474,13 @@ __device__ __forceinline__ void lora_inv_wc(float* inv, const uint8_t* wc, int n
 // four lanes.
 template <int NR, bool F16>
 __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* wc, int n_cta,
-                                                   int N, int r0, int lane) {
+                                                   int N, int r0, int lane, int* status) {
   using H = H16<F16>;
   float inv[NR / 32];
-  lora_inv_wc<NR, F16>(inv, wc, n_cta, N, r0, lane);
+  lora_inv_wc<NR, F16>(inv, wc, n_cta, N, r0, lane, status);
   const int pc = lane & 3;
+  bool inf = false;
+  int inf_n = 0;
 #pragma unroll
   for (int it = 0; it < NR / 8; ++it) {
     const int row = r0 + it * 8 + (lane >> 2);
@@ -463,8 +490,14 @@ __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* w
     x.y = H::pack(__fmul_rn(H::lo(x.y), s), __fmul_rn(H::hi(x.y), s));
     x.z = H::pack(__fmul_rn(H::lo(x.z), s), __fmul_rn(H::hi(x.z), s));
     x.w = H::pack(__fmul_rn(H::lo(x.w), s), __fmul_rn(H::hi(x.w), s));
+    if (has_inf16<F16>(x.x) || has_inf16<F16>(x.y) || has_inf16<F16>(x.z) ||
+        has_inf16<F16>(x.w)) {
+      inf = true;
+      inf_n = n_cta + quad_row(row);
+    }
     *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc) = x;
   }
+  warp_report_lora(status, kStatusLuOverflow, inf, inf_n);
 }
 
 // Direct-load LoRA operands (used when R is not a multiple of 8, so LoRA rows
@@ -500,6 +533,8 @@ __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p,
   const int chunk = lane & 3;
   const int k0 = blk * kLoraRanks + chunk * 8;
   const uint16_t* lu = p.lora_up;
+  bool zero = false, inf = false;
+  int zn = 0, inf_n = 0;
   for (int it = 0; it < NR / 8; ++it) {
     const int row = r0 + it * 8 + (lane >> 2);
     const int n = n_cta + quad_row(row);
@@ -507,6 +542,10 @@ __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p,
     if (n < p.N) {
       const float w = wc ? H16<F16>::one(__ldg(wc + n)) : 1.f;
       inv = (w != 0.f) ? __frcp_rn(w) : 0.f;
+      if (w == 0.f) {
+        zero = true;
+        zn = n;
+      }
     }
     float v[8];
 #pragma unroll
@@ -519,8 +558,15 @@ __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p,
     pk.y = H16<F16>::pack(v[2], v[3]);
     pk.z = H16<F16>::pack(v[4], v[5]);
     pk.w = H16<F16>::pack(v[6], v[7]);
+    if (has_inf16<F16>(pk.x) || has_inf16<F16>(pk.y) || has_inf16<F16>(pk.z) ||
+        has_inf16<F16>(pk.w)) {
+      inf = true;
+      inf_n = n;
+    }
     *reinterpret_cast<uint4*>(dst + sw64_offset(row, chunk)) = pk;
   }
+  warp_report_lora(p.status, kStatusWcscaleZero, zero, zn);
+  warp_report_lora(p.status, kStatusLuOverflow, inf, inf_n);
 }
 
 template <int CG, int BN, int KBI, bool F16, bool SK>
@@ -555,10 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto acc_empty = [&](int a) { return bar0 + 8u * (5 * kMaxStages + 2 + a); };
   const uint32_t never = bar0 + 8u * (5 * kMaxStages + 4);  // no role arrives on it
   auto drain = [&](uint32_t e) { return bar0 + 8u * (5 * kMaxStages + 5 + e); };
+  // issuer e arrives on turn(e) once it has issued an item's MMAs
+  auto turn = [&](uint32_t e) { return bar0 + 8u * (5 * kMaxStages + 7 + e); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * L::kBarCount);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // ring items whose MMAs have been issued (the two issuers take turns)
-  const uint32_t mma_turn = ptx::smem_u32(tmem_slot + 2);
   const Ctl ctl{abort_flag, p.status, p.timeout_ns};
   // Barriers the leader owns, addressed from either CTA of the pair.
   auto to_leader = [&](uint32_t local_bar) {
@@ -581,8 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(never, 1);
     ptx::mbar_init(drain(0), 1);
     ptx::mbar_init(drain(1), 1);
+    ptx::mbar_init(turn(0), 1);
+    ptx::mbar_init(turn(1), 1);
     *abort_flag = 0;
-    ptx::st_volatile_shared(mma_turn, 0u);
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -730,9 +777,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // fall two phases behind on a barrier it tracks by parity.
     // Every MMA accumulates: the epilogue zeroes the accumulator when it has
     // read it (and once before the first tile), so no MMA waits for another to
-    // complete.  The issuers still take turns through a shared-memory word
-    // (no tensor-pipe fence, so nothing drains): the MMAs of successive items
-    // enter the tensor core in ring order and the output is bit-reproducible.
+    // complete.  The issuers still take turns: after issuing item j's MMAs,
+    // its owner executes tcgen05.fence::before_thread_sync and arrives on its
+    // turn barrier (a CTA-scope release); the other issuer waits on that
+    // barrier (acquire) and executes tcgen05.fence::after_thread_sync before
+    // issuing item j + 1.  That orders the MMAs of successive items in ring
+    // order without waiting for any of them to complete, so the fp32
+    // accumulation order, and with it every output bit, is fixed.
     if (lane == 0 && leader) {
       const uint32_t me = warp == 1 ? 0u : 1u;
       int stage = 0;
@@ -806,7 +857,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Items reach the tensor core in ring order: the fp32 accumulation
             // order, and with it every output bit, is the same on every call
             // (unless the caller relaxed the order for the last few percent).
-            if (p.ordered && !wait_turn(mma_turn, j, ctl)) {
+            // Item j - 1 is the other issuer's ((j - 1) >> 1)-th item, i.e. the
+            // completion of that phase of its turn barrier.
+            if (p.ordered && j > 0 &&
+                !wait_bar<false>(turn(me ^ 1u), ((j - 1u) >> 1) & 1u, kSiteMmaTurn, ctl)) {
               ok = false;
               break;
             }
@@ -826,7 +880,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               for (int ks = 0; ks < nsteps; ++ks) step(ks);
             }
-            ptx::st_volatile_shared(mma_turn, j + 1);
+            // Hand the turn over (see above).
+            if (p.ordered) {
+              ptx::tc_fence_before();
+              ptx::mbar_arrive(turn(me));
+            }
             if (CG == 2)
               ptx::mma_commit_pair_multicast(empty(stage), 3);
             else
@@ -886,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              lane);
           else if (p.wcscale != nullptr && !p.prepacked)
             lora_lu_scale_smem<L::kBNc / 2, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N,
-                                                 r0, lane);
+                                                 r0, lane, p.status);
           ptx::fence_proxy_async_smem();
         }
         __syncwarp();
@@ -1009,14 +1067,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
         __threadfence();  // every lane's partial stores are visible device-wide ...
         __syncwarp();     // ... before lane 0 raises the flag
-        if (lane == 0) ptx::st_release_gpu(flag(w.split), p.epoch);
+        if (lane == 0) ptx::st_release_gpu(flag(w.split), 1u);
         continue;
       }
       if (add_partials) {
         bool got = true;
         for (int sp = 0; sp < p.splits - 1 && got; ++sp)
-          got = wait_flag(flag(sp), p.epoch, ctl);
+          got = wait_flag(flag(sp), ctl);
         if (!__all_sync(0xffffffffu, got)) break;
+        // every flag of this warp is up (all lanes have acquired the partials):
+        // lower them for the next launch (the launch boundary orders these
+        // stores before that launch's raises)
+        if (lane == 0)
+          for (int sp = 0; sp < p.splits - 1; ++sp) ptx::st_relaxed_gpu(flag(sp), 0u);
         // fold the other splits' partials into this accumulator (fp32)
         for (int g = g0; g < g0 + kHalfG; ++g) {
           uint32_t v[4][8];
@@ -1040,53 +1103,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
       }
       // Column group g (32 output columns n0 + 32g + 4k + b, k < 8, b < 4) sits in
-      // accumulator columns 128h + 32b + 8(g % 4) + k, h = g / 4.  Each group is
-      // loaded, cleared, scaled, converted, staged and stored as one 32-column
-      // TMA tile; the quadrant's other epilogue warp works on the other half.
-#pragma unroll 1
+      // accumulator columns 128h + 32b + 8(g % 4) + k, h = g / 4; the quadrant's
+      // other epilogue warp works on the other half of the groups.  First every
+      // group of this warp is loaded, cleared, scaled and packed to 16 bits in
+      // registers, and the accumulator goes back to the MMA issuers; only then
+      // are the packed groups staged and stored (one 32-column TMA tile each),
+      // while the next tile accumulates.
+      // The first group goes straight to the staging tile (its previous store
+      // finished reading long ago), the others are held in registers.
+      constexpr int kRegG = kHalfG - 1;
+      uint32_t pk[kRegG > 0 ? kRegG : 1][16];
+      if (lane == 0) ptx::bulk_wait_group_read<0>();
+      __syncwarp();
+#pragma unroll
       for (int gl = 0; gl < kHalfG; ++gl) {
         const int g = g0 + gl;
-        uint32_t cur[4][8];
+        // two halves (accumulator columns 32b.., b = 2h, 2h + 1), so that only
+        // 16 loaded registers are live next to the packed groups
+        uint32_t v[16];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) ptx::tmem_ld_32x32b_x8(gcol(g) + 32 * b, cur[b]);
-        ptx::tmem_wait_ld();
-        // read: clear these columns for the next tile's accumulation
+        for (int h = 0; h < 2; ++h) {
+          uint32_t cur[2][8];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) ptx::tmem_st_32x32b_x8(gcol(g) + 32 * b, zero8);
-        if (gl + 1 == kHalfG) {
-          // this warp's columns are read and cleared: release them to the MMA
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before();
+          for (int b = 0; b < 2; ++b)
+            ptx::tmem_ld_32x32b_x8(gcol(g) + 32 * (2 * h + b), cur[b]);
+          ptx::tmem_wait_ld();
+          // read: clear these columns for the next tile's accumulation
+#pragma unroll
+          for (int b = 0; b < 2; ++b) ptx::tmem_st_32x32b_x8(gcol(g) + 32 * (2 * h + b), zero8);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            // columns 4k + 2h, 4k + 2h + 1 of the group
+            const int o = 32 * gl + 4 * k + 2 * h;
+            const float2 wc2 = *reinterpret_cast<const float2*>(wb + o);
+            const float2 b2 = *reinterpret_cast<const float2*>(wb + BN / 2 + o);
+            const float y0 = fmaf(__uint_as_float(cur[0][k]), wc2.x, b2.x);
+            const float y1 = fmaf(__uint_as_float(cur[1][k]), wc2.y, b2.y);
+            v[2 * k + h] = H::pack(y0, y1);
+          }
+        }
+        if (gl == 0) {
+          stage_row(stg, lane, v);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) pk[gl - 1][x] = v[x];
+        }
+      }
+      // this warp's columns are read and cleared: release them to the MMA
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
+#pragma unroll
+      for (int gl = 0; gl < kHalfG; ++gl) {
+        if (gl > 0) {
+          // the staging tile must no longer be read by the previous store
+          if (lane == 0) ptx::bulk_wait_group_read<0>();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote(acc_empty0 + 8u * acc_stage);
+          stage_row(stg, lane, pk[gl - 1]);
         }
-        // the staging tile must no longer be read by its previous store
-        if (lane == 0) ptx::bulk_wait_group_read<0>();
-        __syncwarp();
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int o = 32 * gl + 4 * k;
-          const float4 wc4 = *reinterpret_cast<const float4*>(wb + o);
-          const float4 bb = *reinterpret_cast<const float4*>(wb + BN / 2 + o);
-          const float y0 = fmaf(__uint_as_float(cur[0][k]), wc4.x, bb.x);
-          const float y1 = fmaf(__uint_as_float(cur[1][k]), wc4.y, bb.y);
-          const float y2 = fmaf(__uint_as_float(cur[2][k]), wc4.z, bb.z);
-          const float y3 = fmaf(__uint_as_float(cur[3][k]), wc4.w, bb.w);
-          pk[2 * k] = H::pack(y0, y1);
-          pk[2 * k + 1] = H::pack(y2, y3);
-        }
-        // 16-byte chunk j of the 64-byte staging row holds columns 8j .. 8j+7
-        // (64-byte swizzle: chunk index XOR bits 1..2 of the row)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(stg + 64 * lane + ((j ^ ((lane >> 1) & 3)) << 4)) =
-              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           // staging row `lane` is output row m_cta + 4 * lane + q
-          ptx::tma_store_3d(&tm_out, ptx::smem_u32(stg), n0 + 32 * g, m_cta / 4, q);
+          ptx::tma_store_3d(&tm_out, ptx::smem_u32(stg), n0 + 32 * (g0 + gl), m_cta / 4, q);
           ptx::bulk_commit_group();
         }
       }

@@ -9,7 +9,9 @@
 //      threads), transposes them in registers and writes 16 bytes.
 //   2. LU' = round16(fp32(LU) * rcp(wcscale)): the correctly rounded fp32
 //      reciprocal and product the fused kernel would otherwise compute per
-//      call, rounded (RNE) into the 16-bit I/O type.
+//      call, rounded (RNE) into the 16-bit I/O type.  A zero wcscale (LU' set
+//      to 0: that column's LoRA term is lost) or an LU' beyond the 16-bit
+//      range is recorded in the device status word, as in the fused kernel.
 #pragma once
 
 #include "svdq_kernel.cuh"
@@ -20,7 +22,7 @@ template <bool F16>
 __global__ void __launch_bounds__(256)
     svdq_prepack_kernel(const uint8_t* __restrict__ wscales, const uint16_t* __restrict__ lu,
                         const uint16_t* __restrict__ wc, uint32_t* __restrict__ wpk,
-                        uint16_t* __restrict__ lup, int N, int K, int R) {
+                        uint16_t* __restrict__ lup, int N, int K, int R, int* status) {
   using H = H16<F16>;
   const long long quads = static_cast<long long>(N / 4);
   const long long n_words = static_cast<long long>(K / 64) * quads;
@@ -55,9 +57,12 @@ __global__ void __launch_bounds__(256)
       if (wc != nullptr) {
         const float w = H::one(__ldg(wc + n));
         inv = (w != 0.f) ? __frcp_rn(w) : 0.f;
+        if (w == 0.f) report_lora_operand(status, kStatusWcscaleZero, n);
       }
       const float v = __fmul_rn(H::one(__ldg(lu + e)), inv);
-      lup[e] = static_cast<uint16_t>(H::pack(v, 0.f) & 0xFFFFu);
+      const uint32_t h = H::pack(v, 0.f);
+      if (has_inf16<F16>(h)) report_lora_operand(status, kStatusLuOverflow, n);
+      lup[e] = static_cast<uint16_t>(h & 0xFFFFu);
     }
   }
 }

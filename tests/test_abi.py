@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, -11, -1):
+    for code in range(0, -13, -1):
         s = binding.status_string(code)
         assert s.startswith("SVDQ_")
     assert binding.status_string(-99) == "SVDQ_ERR_UNKNOWN"

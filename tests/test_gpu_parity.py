@@ -205,10 +205,36 @@ def test_workload_full_matrix(w):
     parity(y, oracle_y(inp, w.M, w.N, w.K, w.R))
 
 
+def sweep_rows(M):
+    """Every 8th row, plus every row of the first and of the last 256-row
+    tile row (all lane quadrants and both CTAs of a pair at both ends)."""
+    rows = set(range(0, M, 8)) | set(range(0, min(256, M))) | set(range(max(0, M - 256), M))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
 @pytest.mark.parametrize("w", synth.sweep_workloads(), ids=lambda w: w.name)
-def test_sweep_sampled_rows(w):
+def test_sweep_rows(w):
+    # the full matrix where the oracle is quick (M <= 4096), else every 8th
+    # row plus the first and last tile rows
     inp = synth.make_workload_inputs(w)
     y = run_gpu(inp, w.M, w.N, w.K, w.R)
-    rows = sample_rows(w.M, 12, seed=w.M)
-    ref = oracle_y(inp, w.M, w.N, w.K, w.R, rows=rows)
-    parity(y[rows], ref)
+    if w.M <= 4096:
+        parity(y, oracle_y(inp, w.M, w.N, w.K, w.R))
+    else:
+        rows = sweep_rows(w.M)
+        parity(y[rows], oracle_y(inp, w.M, w.N, w.K, w.R, rows=rows))
+
+
+# ------------------------------------------------------------ dense calibration
+@pytest.mark.parametrize("cfg", [None] + CONFIGS, ids=["default"] + CFG_IDS)
+def test_dense_calibration_full_matrix(cfg):
+    """The dense calibration variant of the attention projection: R = 0, no
+    wcscale and no bias (1 and 0), through the same kernel -- the block-scaled
+    product alone, every element against the oracle."""
+    w = synth.ATTN_PROJ
+    inp = synth.make_workload_inputs(w)
+    inp["wcscale"] = None
+    inp["bias"] = None
+    inp["lora_act_in"] = None
+    inp["lora_up"] = None
+    full_check(w.M, w.N, w.K, 0, w.seed, options=cfg, inp=inp)

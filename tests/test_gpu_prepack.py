@@ -57,8 +57,16 @@ def test_prepack_kernel_bit_exact(N, K, R, half, wc_kind):
         inp = _edge_weights(inp, half)
     elif wc_kind == "none":
         inp["wcscale"] = None
+    binding.svdq_read_device_status(clear=True)
     d = prepack_gpu(inp, R)
     torch.cuda.synchronize()
+    # a zero wcscale (edge weights, column 5) has no LU' = LU / wcscale: the
+    # prepack writes 0 there and records it in the device status word
+    code, site, _ = binding.svdq_read_device_status(clear=True)
+    if wc_kind == "edge" and R > 0 and N > 5:
+        assert (code, site) == (binding.SVDQ_ERR_WCSCALE_ZERO, 5)
+    else:
+        assert code == 0, (code, site)
     wpk = d["wscales"].cpu().numpy().view(np.uint32)
     assert np.array_equal(wpk, oracle.prepack_wscales(inp["wscales"], N, K))
     want = oracle.prepack_lora_up(inp["lora_up"], inp["wcscale"], N, R, half=half)
