@@ -45,9 +45,10 @@ extern "C" {
                                           LoRA term of that column was dropped, the rest
                                           of out is computed                            */
 #define SVDQ_ERR_LU_OVERFLOW -12       /* device status only: lora_up[n][r] / wcscale[n]
-                                          is beyond the 16-bit I/O type's range for a
-                                          column n (the site): that column's LoRA term is
-                                          infinite, the rest of out is computed         */
+                                          is beyond the 16-bit I/O type's range (or not
+                                          finite) for a column n (the site): that
+                                          column's LoRA term is not finite, the rest of
+                                          out is computed                               */
 
 /* Size of the library's own scratch array (svdq_w4a4_gemm_split_noalloc). */
 #define SVDQ_NOALLOC_SCRATCH_BYTES (16LL << 20)

@@ -359,7 +359,6 @@ struct H16 {
   static __device__ __forceinline__ float hi(uint32_t w) { return bf16_hi(w); }
   static __device__ __forceinline__ uint32_t pack(float a, float b) { return ptx::pack_bf16x2(a, b); }
   static constexpr uint32_t kOnes = 0x3F803F80u;  // (1.0, 1.0)
-  static constexpr uint32_t kInf = 0x7F80u;       // exponent all ones, mantissa 0
 };
 template <>
 struct H16<true> {
@@ -370,13 +369,15 @@ struct H16<true> {
   static __device__ __forceinline__ float hi(uint32_t w) { return one(uint16_t(w >> 16)); }
   static __device__ __forceinline__ uint32_t pack(float a, float b) { return ptx::pack_f16x2(a, b); }
   static constexpr uint32_t kOnes = 0x3C003C00u;
-  static constexpr uint32_t kInf = 0x7C00u;
 };
 
-// Either 16-bit half of a packed pair is +-infinity.
+// Non-zero iff either half of a packed 16-bit pair has an all-ones exponent
+// (infinite or NaN); branch-free for the hot loops.  Adding the exponent's lowest bit to
+// the magnitude carries into bit 15 exactly then; no carry crosses halves.
 template <bool F16>
-__device__ __forceinline__ bool has_inf16(uint32_t w) {
-  return ((w & 0x7FFFu) == H16<F16>::kInf) || (((w >> 16) & 0x7FFFu) == H16<F16>::kInf);
+__device__ __forceinline__ uint32_t nonfinite16_bits(uint32_t w) {
+  constexpr uint32_t kInc = F16 ? 0x04000400u : 0x00800080u;
+  return ((w & 0x7FFF7FFFu) + kInc) & 0x80008000u;
 }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
@@ -446,41 +447,38 @@ __device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* r
 }
 
 // 1/wcscale for tile rows r0 + lane + 32t (t < NR/32), 0 outside N or for a
-// zero wcscale (fp32 reciprocal, correctly rounded; a zero inside N is
-// reported in the status word).
+// zero wcscale (fp32 reciprocal, correctly rounded).  zero_col: a column
+// inside N with a zero wcscale, else unchanged (-1).
 template <int NR, bool F16>
 __device__ __forceinline__ void lora_inv_wc(float* inv, const uint8_t* wc, int n_cta, int N,
-                                            int r0, int lane, int* status) {
-  bool zero = false;
-  int zn = 0;
+                                            int r0, int lane, int& zero_col) {
 #pragma unroll
   for (int t = 0; t < NR / 32; ++t) {
     const int off = quad_row(r0 + lane + 32 * t);
     const float w = H16<F16>::one(*reinterpret_cast<const uint16_t*>(wc + 2 * off));
     const bool in = n_cta + off < N;
     inv[t] = (in && w != 0.f) ? __frcp_rn(w) : 0.f;
-    if (in && w == 0.f) {
-      zero = true;
-      zn = n_cta + off;
-    }
+    zero_col = (in && w == 0.f) ? n_cta + off : zero_col;
   }
-  warp_report_lora(status, kStatusWcscaleZero, zero, zn);
 }
 
 // LU' rows r0 .. r0+NR-1 in place: every 16-byte chunk of tile row r (column
 // n = n_cta + quad_row(r)) times 1/wcscale[n] (fp32 product, bf16 RNE); the
 // staged wcscale is in plain column order.  Rows outside N (zero-filled) stay
 // zero.  Each row's reciprocal is computed once and shuffled to the row's
-// four lanes.
+// four lanes.  zero_col / bad_col (-1 if none): a column with a zero wcscale,
+// a column whose LU' is not finite; the caller reports them once its ring
+// arrival is made (the checks are branch-free, off the ring's path).
 template <int NR, bool F16>
 __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* wc, int n_cta,
-                                                   int N, int r0, int lane, int* status) {
+                                                   int N, int r0, int lane, int& zero_col,
+                                                   int& bad_col) {
   using H = H16<F16>;
   float inv[NR / 32];
-  lora_inv_wc<NR, F16>(inv, wc, n_cta, N, r0, lane, status);
+  lora_inv_wc<NR, F16>(inv, wc, n_cta, N, r0, lane, zero_col);
   const int pc = lane & 3;
-  bool inf = false;
-  int inf_n = 0;
+  uint32_t any_bad = 0u;
+  int bad_row = 0;
 #pragma unroll
   for (int it = 0; it < NR / 8; ++it) {
     const int row = r0 + it * 8 + (lane >> 2);
@@ -490,14 +488,13 @@ __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* w
     x.y = H::pack(__fmul_rn(H::lo(x.y), s), __fmul_rn(H::hi(x.y), s));
     x.z = H::pack(__fmul_rn(H::lo(x.z), s), __fmul_rn(H::hi(x.z), s));
     x.w = H::pack(__fmul_rn(H::lo(x.w), s), __fmul_rn(H::hi(x.w), s));
-    if (has_inf16<F16>(x.x) || has_inf16<F16>(x.y) || has_inf16<F16>(x.z) ||
-        has_inf16<F16>(x.w)) {
-      inf = true;
-      inf_n = n_cta + quad_row(row);
-    }
+    const uint32_t b = nonfinite16_bits<F16>(x.x) | nonfinite16_bits<F16>(x.y) |
+                       nonfinite16_bits<F16>(x.z) | nonfinite16_bits<F16>(x.w);
+    any_bad |= b;
+    bad_row = b ? row : bad_row;
     *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc) = x;
   }
-  warp_report_lora(status, kStatusLuOverflow, inf, inf_n);
+  bad_col = any_bad ? n_cta + quad_row(bad_row) : bad_col;
 }
 
 // Direct-load LoRA operands (used when R is not a multiple of 8, so LoRA rows
@@ -526,15 +523,14 @@ __device__ __forceinline__ void lora_la_direct(uint8_t* dst, const KParams& p, i
 }
 
 // `wc` is NULL for a prepacked LU' (already divided) or an absent wcscale.
+// zero_col / bad_col as for lora_lu_scale_smem.
 template <int NR, bool F16>
 __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p,
                                                const uint16_t* wc, int n_cta, int blk, int r0,
-                                               int lane) {
+                                               int lane, int& zero_col, int& bad_col) {
   const int chunk = lane & 3;
   const int k0 = blk * kLoraRanks + chunk * 8;
   const uint16_t* lu = p.lora_up;
-  bool zero = false, inf = false;
-  int zn = 0, inf_n = 0;
   for (int it = 0; it < NR / 8; ++it) {
     const int row = r0 + it * 8 + (lane >> 2);
     const int n = n_cta + quad_row(row);
@@ -542,10 +538,7 @@ __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p,
     if (n < p.N) {
       const float w = wc ? H16<F16>::one(__ldg(wc + n)) : 1.f;
       inv = (w != 0.f) ? __frcp_rn(w) : 0.f;
-      if (w == 0.f) {
-        zero = true;
-        zn = n;
-      }
+      zero_col = (w == 0.f) ? n : zero_col;
     }
     float v[8];
 #pragma unroll
@@ -558,15 +551,11 @@ __device__ __forceinline__ void lora_lu_direct(uint8_t* dst, const KParams& p,
     pk.y = H16<F16>::pack(v[2], v[3]);
     pk.z = H16<F16>::pack(v[4], v[5]);
     pk.w = H16<F16>::pack(v[6], v[7]);
-    if (has_inf16<F16>(pk.x) || has_inf16<F16>(pk.y) || has_inf16<F16>(pk.z) ||
-        has_inf16<F16>(pk.w)) {
-      inf = true;
-      inf_n = n;
-    }
+    const uint32_t b = nonfinite16_bits<F16>(pk.x) | nonfinite16_bits<F16>(pk.y) |
+                       nonfinite16_bits<F16>(pk.z) | nonfinite16_bits<F16>(pk.w);
+    bad_col = b ? n : bad_col;
     *reinterpret_cast<uint4*>(dst + sw64_offset(row, chunk)) = pk;
   }
-  warp_report_lora(p.status, kStatusWcscaleZero, zero, zn);
-  warp_report_lora(p.status, kStatusLuOverflow, inf, inf_n);
 }
 
 template <int CG, int BN, int KBI, bool F16, bool SK>
@@ -934,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        int zero_col = -1, bad_col = -1;
         if (i < w.lora) {
           // LU' rows [h kBNc/2, (h+1) kBNc/2) (the scale feeders build LA')
           uint8_t* st = smem + stage * L::kStageBytes;
@@ -941,10 +931,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!p.lora_tma)
             lora_lu_direct<L::kBNc / 2, F16>(st + L::kLoraLU, p,
                                              p.prepacked ? nullptr : p.wcscale, n_cta, i, r0,
-                                             lane);
+                                             lane, zero_col, bad_col);
           else if (p.wcscale != nullptr && !p.prepacked)
             lora_lu_scale_smem<L::kBNc / 2, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N,
-                                                 r0, lane, p.status);
+                                                 r0, lane, zero_col, bad_col);
           ptx::fence_proxy_async_smem();
         }
         __syncwarp();
@@ -952,6 +942,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // leader's MMA reads: the proxy fence above orders them before this
         // arrival (CTA-scope release, as for every other arrival here).
         if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
+        // LoRA operands the accumulator cannot carry, reported after the
+        // arrival so that the ring does not wait for it
+        if (i < w.lora) {
+          warp_report_lora(p.status, kStatusWcscaleZero, zero_col >= 0, zero_col);
+          warp_report_lora(p.status, kStatusLuOverflow, bad_col >= 0, bad_col);
+        }
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(256)
       }
       const float v = __fmul_rn(H::one(__ldg(lu + e)), inv);
       const uint32_t h = H::pack(v, 0.f);
-      if (has_inf16<F16>(h)) report_lora_operand(status, kStatusLuOverflow, n);
+      if (nonfinite16_bits<F16>(h & 0xFFFFu)) report_lora_operand(status, kStatusLuOverflow, n);
       lup[e] = static_cast<uint16_t>(h & 0xFFFFu);
     }
   }
