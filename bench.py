@@ -36,7 +36,10 @@ the same way (flushed L2, per-launch events, 10 launches each), and under
 attention projection, MLP-up and MLP-down, each on the default route, the
 dense calibration variant (R = 0, no wcscale / bias) and the prepacked +
 packed-scale route, and the 24-case token-count sweep (default route, plus
-the split-K entry point where the planner splits).  The headline `value` is
+the split-K entry point where the planner splits); then the activation
+quantiser on the production activations (GB/s against the measured HBM copy
+bandwidth) and the whole layer from 16-bit activations (quantiser with
+packed scales + prepacked operator in one event pair).  The headline `value` is
 the attention projection, the configuration the metric is quoted on.
 `--no-per-shape` skips that section.
 """
@@ -390,10 +393,73 @@ def run_per_shape(pkg, synth, torch, dev, stream, flush, fp4_peak):
                     "how": "svdq_w4a4_gemm per case (and svdq_w4a4_gemm_split where the planner "
                            "splits; the summary takes the faster), 2 warm-up + 5 timed flushed "
                            "launches"}
+    res.update(run_quantize_shapes(pkg, synth, torch, dev, stream, flush, fp4_peak))
     code, site, _ = pkg.svdq_read_device_status(clear=True)
     if code != 0:
         raise RuntimeError(f"device status {code} at wait site {site} in the per-shape runs")
     return res
+
+
+def quant_bytes(M, K, R):
+    """Algorithmic HBM bytes of one quantiser call: x and lora_down read once,
+    codes, scales and lora_act_in written once."""
+    return 2 * M * K + 2 * R * K + M * K // 2 + M * K // 16 + 4 * M * R
+
+
+def run_quantize_shapes(pkg, synth, torch, dev, stream, flush, fp4_peak):
+    """The activation quantiser on the production activations (HBM-bound:
+    GB/s against the measured copy bandwidth), and the whole layer from 16-bit
+    activations: quantiser (packed scales) + prepacked operator, one event pair."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            hbm, hbm_src = float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        hbm, hbm_src = 6800.0, "fallback"
+    quant = {}
+    for name, M, K, R in (("x_4096x3072_r32", 4096, 3072, 32),
+                          ("x_4096x12288_r128", 4096, 12288, 128)):
+        a = synth.make_activations(M, K, R, seed=7)
+        x, ld = a["x"].to(dev), a["lora_down"].to(dev)
+        nbytes = quant_bytes(M, K, R)
+        e = {"M": M, "K": K, "R": R, "bytes": nbytes, "plan": pkg.svdq_quantize_query(M, K, R)}
+        for packed in (False, True):
+            outs = pkg.svdq_quantize_act(x, ld, scales_packed=packed)
+            ms = time_flushed(lambda: pkg.svdq_quantize_act(x, ld, *outs, scales_packed=packed,
+                                                            stream=stream),
+                              flush, stream, 3, 10, torch, dev)
+            mean = statistics.mean(ms)
+            gbs = nbytes / (mean * 1e-3) / 1e9
+            e["packed_scales" if packed else "raw_scales"] = {
+                "ms_mean": mean, "ms_median": statistics.median(ms), "ms_min": min(ms),
+                "gbs": gbs, "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm,
+                                         "unit": "GB/s", "frac": gbs / hbm,
+                                         "peak_source": f"{hbm_src} copy bandwidth"}}
+            del outs
+        quant[name] = e
+        del x, ld
+    layer = {}
+    for w in (synth.ATTN_PROJ, synth.MLP_UP, synth.MLP_DOWN):
+        inp = synth.make_workload_inputs(w)
+        d = {k: v.to(dev) for k, v in inp.items()}
+        a = synth.make_activations(w.M, w.K, w.R, seed=w.seed + 100)
+        x, ld = a["x"].to(dev), a["lora_down"].to(dev)
+        wpk, lup = pkg.svdq_prepack_weights(d["wscales"], d["lora_up"], d["wcscale"])
+        act, apk, la = pkg.svdq_quantize_act(x, ld, scales_packed=True)
+        out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        o2 = dict(act_scales_packed=1)
+
+        def call_layer():
+            pkg.svdq_quantize_act(x, ld, act, apk, la, scales_packed=True, stream=stream)
+            pkg.svdq_w4a4_gemm_prepacked(act, d["wgt"], apk, wpk, la, lup, d["wcscale"],
+                                         d["bias"], out, stream=stream, options=o2)
+        e = shape_entry(float(w.flops), time_flushed(call_layer, flush, stream, 3, 10, torch,
+                                                     dev), fp4_peak)
+        e["how"] = ("svdq_quantize_act (packed scales) + svdq_w4a4_gemm_prepacked "
+                    "(act_scales_packed) in one event pair; tflops counts the operator's "
+                    "2MNK + 2MNR")
+        layer[w.name] = e
+        del d, x, ld, wpk, lup, act, apk, la, out
+    return {"quantize": quant, "layer_from_16bit_x": layer}
 
 
 def run_ours(args, w, rank, world, local_rank):

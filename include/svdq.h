@@ -198,6 +198,60 @@ int svdq_prepack_weights(const void* wscales, const void* lora_up, const void* w
 int svdq_pack_scales(const void* scales, int64_t rows, int64_t K, void* packed, void* stream);
 
 /*
+ * svdq_quantize_act -- the operator's activation inputs from 16-bit
+ * activations, in one pass over x ("SVDQuant W4A4 on Blackwell" §1: the W4A4
+ * operator is the compute-bound half of SVDQuant, fed by an activation
+ * quantiser; §2: act, ascales and lora_act_in, in the formats of §3.1; §3.3:
+ * LA is the LoRA-down activation).  The page names this producer but does not
+ * define it; the library takes the plain NVFP4 reading, per group of 16
+ * consecutive k in a row m (single-level scaling, as everywhere here):
+ *
+ *     amax             = max |x[m, k]| over the group
+ *     ascales[g][m]    = E4M3(amax / 6), rounded to nearest even, saturating
+ *                        at 448; the scale s is that byte's value
+ *     code(m, k)       = E2M1(x[m, k] / s), rounded to nearest even (ties to
+ *                        the even code), saturating at +-6; every code of the
+ *                        group is 0 when s == 0; a code of magnitude 0 is +0
+ *     lora_act_in[m,r] = sum_k x[m, k] * lora_down[r, k]   (fp32 result)
+ *
+ * The rounding decisions are those of the exact quotients amax / 6 and x / s
+ * (the kernel's fp32 arithmetic reaches the same codes for 16-bit x).
+ *
+ * x             device, 16-bit [M, K] row-major (io_dtype: bf16 or fp16), finite.
+ * lora_down     device, same 16-bit type [R, K] row-major; NULL iff R == 0.
+ * M, K, R       M a multiple of 16, K a positive multiple of 64, 0 <= R <= 128,
+ *               within the size limits above.  M == 0 returns SVDQ_OK without
+ *               touching any pointer (which may then be NULL).
+ * io_dtype      SVDQ_IO_BF16 or SVDQ_IO_FP16.
+ * scales_packed 0: ascales is uint8 [K/16, M] (svdq_w4a4_gemm's layout);
+ *               1: uint32 [K/64, M] words, word (s, m) byte g = scale of group
+ *               4s + g (svdq_pack_scales' layout, for act_scales_packed).
+ * act           device, uint8 [M, K/2]: low nibble = even k.
+ * ascales       device, as selected by scales_packed.
+ * lora_act_in   device, fp32 [M, R]; NULL iff R == 0.  Accumulated in fp32 on
+ *               the tensor cores from the 16-bit products; with several CTAs
+ *               per 128-row tile their fp32 partials are added in a fixed
+ *               order, so the same call gives the same bits every time.
+ * stream        a cudaStream_t.
+ *
+ * Every pointer must be 16-byte aligned; outputs must not overlap inputs or
+ * each other.  Asynchronous on `stream`, allocates nothing, never
+ * synchronises.  A bounded wait that expires records SVDQ_ERR_TIMEOUT in the
+ * device status word.
+ */
+int svdq_quantize_act(const void* x, const void* lora_down, int64_t M, int64_t K, int64_t R,
+                      int32_t io_dtype, int32_t scales_packed, void* act, void* ascales,
+                      float* lora_act_in, void* stream);
+
+/* The launch svdq_quantize_act would make (host only; touches no device when
+ * sm_count > 0): CTAs per 128-row tile along K (*splits, 1, 2, 4 or 8: a
+ * cluster that adds its LoRA-down partials in distributed shared memory),
+ * total CTAs, ring stages and dynamic shared memory per CTA.  Any output
+ * pointer may be NULL.  sm_count <= 0 plans for the current device. */
+int svdq_quantize_query(int64_t M, int64_t K, int64_t R, int32_t sm_count, int32_t* splits,
+                        int32_t* grid, int32_t* stages, int32_t* smem_bytes);
+
+/*
  * svdq_w4a4_gemm_prepacked -- svdq_w4a4_gemm_ex on prepacked weights: the
  * same operator and result, with wscales_packed and lora_up_packed from
  * svdq_prepack_weights in place of wscales and lora_up.  wcscale must be the
@@ -355,7 +409,7 @@ const char* svdq_status_string(int status);
 /* Library ABI version (major * 10000 + minor * 100 + patch).  The structs
  * above grow only at their end; a caller built against a header with another
  * major.minor (SVDQ_ABI_VERSION / 100) must not pass them to this library. */
-#define SVDQ_ABI_VERSION 500
+#define SVDQ_ABI_VERSION 600
 int svdq_version(void);
 
 #ifdef __cplusplus

@@ -15,7 +15,7 @@ from typing import Optional
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsvdq.so")
 # include/svdq.h SVDQ_ABI_VERSION the structs below mirror
-ABI_VERSION = 500
+ABI_VERSION = 600
 # include/svdq.h size limits
 SVDQ_MAX_MN = 1 << 24
 SVDQ_MAX_K = 1 << 20
@@ -44,7 +44,7 @@ EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_prepack_weights", "svdq
             "svdq_w4a4_gemm_prepacked", "svdq_w4a4_gemm_split", "svdq_w4a4_gemm_split_noalloc",
             "svdq_workspace_size",
             "svdq_query_plan", "svdq_lora_stage_bytes", "svdq_read_device_status",
-            "svdq_status_string", "svdq_version")
+            "svdq_status_string", "svdq_version", "svdq_quantize_act", "svdq_quantize_query")
 
 
 class SvdqOptions(ctypes.Structure):
@@ -128,6 +128,10 @@ def load(path: Optional[str] = None):
         lib.svdq_status_string.argtypes = [ctypes.c_int]
         lib.svdq_version.restype = ctypes.c_int
         lib.svdq_version.argtypes = []
+        lib.svdq_quantize_act.restype = ctypes.c_int
+        lib.svdq_quantize_act.argtypes = [vp, vp] + [i64] * 3 + [i32] * 2 + [vp] * 4
+        lib.svdq_quantize_query.restype = ctypes.c_int
+        lib.svdq_quantize_query.argtypes = [i64] * 3 + [i32] + [ctypes.POINTER(i32)] * 4
         # the ctypes structs here mirror include/svdq.h at ABI_VERSION
         if lib.svdq_version() // 100 != ABI_VERSION // 100:
             raise RuntimeError(f"{p} has ABI version {lib.svdq_version()}, this binding "
@@ -377,3 +381,57 @@ def svdq_read_device_status(clear: bool = True):
 
 def svdq_version() -> int:
     return int(load().svdq_version())
+
+
+def svdq_quantize_act(x, lora_down=None, act=None, ascales=None, lora_act_in=None,
+                      scales_packed: bool = False, stream=None, check: bool = True):
+    """The operator's activation inputs from 16-bit activations x [M, K]
+    (bf16 or fp16): returns (act uint8 [M, K/2], ascales uint8 [K/16, M] or
+    int32 words [K/64, M] with ``scales_packed``, lora_act_in fp32 [M, R] or
+    None).  lora_down is [R, K] in x's type, or None for R = 0.  Outputs are
+    allocated here unless given.  Asynchronous on ``stream``."""
+    import torch
+
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("x must be bf16 or fp16")
+    _check("x", x, x.dtype)
+    M, K = x.shape
+    R = 0 if lora_down is None else int(lora_down.shape[0])
+    if R:
+        _check("lora_down", lora_down, x.dtype)
+        if tuple(lora_down.shape) != (R, K):
+            raise ValueError("lora_down must be [R, K]")
+    dev = x.device
+    if act is None:
+        act = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    sc_dt, sc_shape = (torch.int32, (K // 64, M)) if scales_packed else (torch.uint8, (K // 16, M))
+    if ascales is None:
+        ascales = torch.empty(sc_shape, dtype=sc_dt, device=dev)
+    if R and lora_act_in is None:
+        lora_act_in = torch.empty((M, R), dtype=torch.float32, device=dev)
+    _check("act", act, torch.uint8)
+    _check("ascales", ascales, sc_dt)
+    if tuple(act.shape) != (M, K // 2) or tuple(ascales.shape) != sc_shape:
+        raise ValueError("inconsistent output shapes")
+    if R:
+        _check("lora_act_in", lora_act_in, torch.float32)
+        if tuple(lora_act_in.shape) != (M, R):
+            raise ValueError("lora_act_in must be [M, R]")
+    io = SVDQ_IO_FP16 if x.dtype == torch.float16 else SVDQ_IO_BF16
+    h = _stream_handle(stream, dev)
+    with torch.cuda.device(dev):
+        rc = load().svdq_quantize_act(_ptr(x), _ptr(lora_down) if R else None, M, K, R, io,
+                                      1 if scales_packed else 0, _ptr(act), _ptr(ascales),
+                                      _ptr(lora_act_in) if R else None, h)
+    if check and rc != SVDQ_OK:
+        raise SvdqError(rc, "svdq_quantize_act")
+    return act, ascales, (lora_act_in if R else None)
+
+
+def svdq_quantize_query(M: int, K: int, R: int, sm_count: int = 0) -> dict:
+    """The quantiser's launch: K splits per row tile, CTAs, stages, smem bytes."""
+    v = [ctypes.c_int32() for _ in range(4)]
+    rc = load().svdq_quantize_query(M, K, R, sm_count, *[ctypes.byref(t) for t in v])
+    if rc != SVDQ_OK:
+        raise SvdqError(rc, "svdq_quantize_query")
+    return dict(zip(("splits", "grid", "stages", "smem_bytes"), (int(t.value) for t in v)))

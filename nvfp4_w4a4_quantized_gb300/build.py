@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libsvdq.so")
 SOURCES = [os.path.join(CSRC, "svdq_api.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("svdq_kernel.cuh", "svdq_prepack.cuh", "ptx.cuh")] + [
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("svdq_kernel.cuh", "svdq_prepack.cuh", "svdq_quant.cuh", "ptx.cuh")] + [
     os.path.join(INCLUDE, "svdq.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -5,6 +5,8 @@
 // descriptors); the kernel's one-hot GPU tests pin the layouts empirically.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include <cstdint>
 
 namespace svdq {
@@ -402,6 +404,72 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+
+// ---------------------------------------------------------------- NVFP4 conversions
+// Eight fp32 values -> four bytes of E2M1 code pairs: byte i holds v[2i] in
+// bits 0..3 and v[2i + 1] in bits 4..7 (cvt's first source goes to the upper
+// nibble); round to nearest even, saturating at +-6.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float* v) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
+        "f"(v[7]));
+  return r;
+}
+
+// fp32 -> FP8-E4M3 byte, round to nearest even, saturating at 448 (both bytes
+// of the pair get the same value, so the byte order does not matter).
+__device__ __forceinline__ uint32_t cvt_e4m3(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(v));
+  return r & 0xFFu;
+}
+
+// Value of an FP8-E4M3 byte (exact in fp16, hence in fp32).
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  uint32_t h2;
+  const uint16_t pair = static_cast<uint16_t>(b | (b << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// Packed fp32 pairs (sm_100 family): {lo, hi} in one 64-bit register.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// Halfword-wise max(|a|, |b|) of two 16-bit float pairs (bf16 or fp16); the
+// sign bit of each result is sign(a) xor sign(b), to be cleared by the caller.
+template <bool F16>
+__device__ __forceinline__ uint32_t maxabs16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if (F16)
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  else
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 

@@ -14,6 +14,7 @@
 #include "svdq.h"
 #include "svdq_kernel.cuh"
 #include "svdq_prepack.cuh"
+#include "svdq_quant.cuh"
 
 namespace svdq {
 
@@ -45,6 +46,7 @@ struct DeviceInfo {
   // then those six with split-K
   bool attr_set[12] = {};
   int max_clusters[12] = {};
+  int quant_smem_set[2] = {};  // activation quantiser (bf16, fp16): opted-in smem bytes
 };
 
 std::mutex g_mutex;
@@ -611,6 +613,131 @@ int run_gemm(const void* act, const void* wgt, const void* ascales, const void* 
             : launch_any<false, false>(pl, dinfo, op, kp, M, N, K, R, s);
 }
 
+
+// ---------------------------------------------------------------- activation quantiser
+struct QuantPlan {
+  int tiles = 0, splits = 1, stages = 0, r16 = 0, tmem_cols = 0, smem = 0, chunks = 0;
+};
+
+// One CTA per 128-row tile and K range.  A row tile is split along K over a
+// cluster of 2, 4 or 8 CTAs while the tiles alone would leave SMs idle (each
+// CTA streams its own part of x; the LoRA-down partials are added inside the
+// cluster).  Ring depth: as many 64-wide K chunks as fit, up to ten: a chunk's
+// round trip (HBM latency under load, then the quantisers) is about 2.5 us,
+// and covering it at 50 GB/s per SM takes well over 100 KB in flight.
+int plan_quant(int64_t M, int64_t K, int64_t R, int sm_count, int smem_optin, QuantPlan* q) {
+  q->tiles = static_cast<int>((M + kQRows - 1) / kQRows);
+  q->chunks = static_cast<int>(K / kQChunk);
+  q->splits = 1;
+  while (2 * q->splits <= kQMaxSplits && 2 * q->splits <= q->chunks &&
+         static_cast<long long>(q->tiles) * 2 * q->splits <= sm_count)
+    q->splits *= 2;
+  q->r16 = R > 0 ? static_cast<int>((R + 15) / 16 * 16) : 0;
+  q->tmem_cols = 0;
+  if (q->r16 > 0) {
+    q->tmem_cols = 32;
+    while (q->tmem_cols < q->r16) q->tmem_cols *= 2;
+  }
+  const int room = smem_optin - quant_smem_bytes(q->r16, 0);
+  q->stages = room / quant_stage_bytes(q->r16);
+  if (q->stages > 10) q->stages = 10;
+  if (q->stages < 3 || q->stages * quant_stage_bytes(q->r16) < quant_part_bytes(q->r16))
+    return SVDQ_ERR_CUDA;
+  q->smem = quant_smem_bytes(q->r16, q->stages);
+  return SVDQ_OK;
+}
+
+template <bool F16>
+int launch_quant(const QuantPlan& qp, DeviceInfo* dinfo, const void* x, const void* ld,
+                 int64_t M, int64_t K, int64_t R, int packed, void* act, void* ascales,
+                 float* la, cudaStream_t stream) {
+  constexpr CUtensorMapDataType kIoType =
+      F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  auto kern = svdq_quant_kernel<F16>;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int& set = dinfo->quant_smem_set[F16 ? 1 : 0];
+    if (set < qp.smem) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, qp.smem) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        return SVDQ_ERR_CUDA;
+      }
+      set = qp.smem;
+    }
+  }
+  int rc = SVDQ_OK;
+  alignas(64) CUtensorMap tm[2];
+  // x [M][K] and lora_down [R][K]: 64-element (128-byte) boxes of 128 and R16
+  // rows with the 128-byte swizzle the MMA descriptors expect
+  const uint64_t d_x[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)},
+                 s_x[1] = {static_cast<uint64_t>(K) * 2};
+  const uint32_t b_x[2] = {kQChunk, kQRows};
+  if ((rc = encode(&tm[0], kIoType, 2, x, d_x, s_x, b_x, CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
+    return rc;
+  if (R > 0) {
+    const uint64_t d_ld[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(R)};
+    const uint32_t b_ld[2] = {kQChunk, static_cast<uint32_t>(qp.r16)};
+    if ((rc = encode(&tm[1], kIoType, 2, ld, d_ld, s_x, b_ld, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        SVDQ_OK)
+      return rc;
+  } else {
+    tm[1] = tm[0];  // unused
+  }
+  QParams p{};
+  p.act = static_cast<uint8_t*>(act);
+  p.ascales = static_cast<uint8_t*>(ascales);
+  p.la = la;
+  p.M = static_cast<int>(M);
+  p.K = static_cast<int>(K);
+  p.R = static_cast<int>(R);
+  p.r16 = qp.r16;
+  p.chunks = qp.chunks;
+  p.splits = qp.splits;
+  p.stages = qp.stages;
+  p.packed = packed;
+  p.tmem_cols = qp.tmem_cols;
+  p.status = dinfo->status;
+  p.timeout_ns = static_cast<unsigned long long>(kDefaultTimeoutMs) * 1000000ull;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(qp.tiles * qp.splits));
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = qp.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(qp.splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = qp.splits > 1 ? 2 : 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm[0], tm[1], p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return SVDQ_ERR_LAUNCH;
+  }
+  return SVDQ_OK;
+}
+
+int validate_quant(const void* x, const void* ld, int64_t M, int64_t K, int64_t R,
+                   int32_t io_dtype, int32_t packed, const void* act, const void* ascales,
+                   const float* la) {
+  if (io_dtype != SVDQ_IO_BF16 && io_dtype != SVDQ_IO_FP16) return SVDQ_ERR_BAD_OPTION;
+  if (packed != 0 && packed != 1) return SVDQ_ERR_BAD_OPTION;
+  if (M < 0 || K <= 0 || R < 0) return SVDQ_ERR_INVALID_ARG;
+  if (M % 16 || K % 64 || M > SVDQ_MAX_MN || K > SVDQ_MAX_K || R > SVDQ_MAX_RANK)
+    return SVDQ_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return SVDQ_OK;  // nothing to read or write (empty tensors may be NULL)
+  if (!x || !act || !ascales) return SVDQ_ERR_INVALID_ARG;
+  if ((R > 0) != (ld != nullptr) || (R > 0) != (la != nullptr)) return SVDQ_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, ld, act, ascales, la};
+  for (const void* q : ptrs)
+    if (q && !aligned(q, 16)) return SVDQ_ERR_MISALIGNED;
+  return SVDQ_OK;
+}
+
 }  // namespace
 }  // namespace svdq
 
@@ -885,4 +1012,51 @@ extern "C" int svdq_w4a4_gemm_split_noalloc(const void* act, const void* wgt, co
   return run_gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, M, N, K,
                   R, options, stream, weights_prepacked == 1, d->noalloc_scratch,
                   SVDQ_NOALLOC_SCRATCH_BYTES);
+}
+
+extern "C" int svdq_quantize_act(const void* x, const void* lora_down, int64_t M, int64_t K,
+                                 int64_t R, int32_t io_dtype, int32_t scales_packed, void* act,
+                                 void* ascales, float* lora_act_in, void* stream) {
+  using namespace svdq;
+  int rc = validate_quant(x, lora_down, M, K, R, io_dtype, scales_packed, act, ascales,
+                          lora_act_in);
+  if (rc != SVDQ_OK) return rc;
+  if (M == 0) return SVDQ_OK;
+  int dev = 0;
+  DeviceInfo* dinfo = nullptr;
+  if ((rc = probe_device(&dev, &dinfo)) != SVDQ_OK) return rc;
+  QuantPlan qp;
+  if ((rc = plan_quant(M, K, R, dinfo->sm_count, dinfo->smem_optin, &qp)) != SVDQ_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return io_dtype == SVDQ_IO_FP16
+             ? launch_quant<true>(qp, dinfo, x, lora_down, M, K, R, scales_packed, act, ascales,
+                                  lora_act_in, s)
+             : launch_quant<false>(qp, dinfo, x, lora_down, M, K, R, scales_packed, act, ascales,
+                                   lora_act_in, s);
+}
+
+extern "C" int svdq_quantize_query(int64_t M, int64_t K, int64_t R, int32_t sm_count,
+                                   int32_t* splits, int32_t* grid, int32_t* stages,
+                                   int32_t* smem_bytes) {
+  using namespace svdq;
+  if (M < 0 || K <= 0 || R < 0) return SVDQ_ERR_INVALID_ARG;
+  if (M % 16 || K % 64 || M > SVDQ_MAX_MN || K > SVDQ_MAX_K || R > SVDQ_MAX_RANK)
+    return SVDQ_ERR_UNSUPPORTED_SHAPE;
+  int sms = sm_count, optin = kGb300SmemOptin;
+  if (sms <= 0) {
+    int dev = 0;
+    DeviceInfo* dinfo = nullptr;
+    const int rc = probe_device(&dev, &dinfo);
+    if (rc != SVDQ_OK) return rc;
+    sms = dinfo->sm_count;
+    optin = dinfo->smem_optin;
+  }
+  QuantPlan qp;
+  const int rc = plan_quant(M, K, R, sms, optin, &qp);
+  if (rc != SVDQ_OK) return rc;
+  if (splits) *splits = qp.splits;
+  if (grid) *grid = qp.tiles * qp.splits;
+  if (stages) *stages = qp.stages;
+  if (smem_bytes) *smem_bytes = qp.smem;
+  return SVDQ_OK;
 }

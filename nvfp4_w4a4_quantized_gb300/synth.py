@@ -18,6 +18,13 @@ Distributions (the benchmark workloads' recipe):
   wcscale        bf16 U(0.5, 2)          [N]
   bias           bf16 N(0, 0.1)          [N]
 drawn in exactly that order from one seeded CPU torch.Generator.
+
+Activations for the activation quantiser (make_activations), drawn in this
+order from their own seeded generator:
+  channel scale  2^u per input channel k, u ~ U{-2..2} (the per-channel
+                 magnitudes smoothing leaves in activations)
+  x              16-bit N(0, 1) * channel scale   [M, K]
+  lora_down      16-bit N(0, 1/K)                 [R, K]
 """
 
 from __future__ import annotations
@@ -110,3 +117,16 @@ def make_inputs(M: int, N: int, K: int, R: int, seed: int,
 
 def make_workload_inputs(w: Workload) -> Dict[str, torch.Tensor]:
     return make_inputs(w.M, w.N, w.K, w.R, w.seed)
+
+
+def make_activations(M: int, K: int, R: int, seed: int,
+                     half: bool = False) -> Dict[str, torch.Tensor]:
+    """16-bit activations x [M, K] and the LoRA down-projection [R, K] (bf16,
+    or fp16 with ``half``) as contiguous CPU tensors (module docstring)."""
+    h16 = torch.float16 if half else torch.bfloat16
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    chan = torch.exp2(torch.randint(-2, 3, (K,), generator=g).to(torch.float32))
+    x = (torch.randn((M, K), generator=g, dtype=torch.float32) * chan).to(h16)
+    lora_down = (torch.randn((R, K), generator=g, dtype=torch.float32) * K ** -0.5).to(h16)
+    return dict(x=x.contiguous(), lora_down=lora_down.contiguous())

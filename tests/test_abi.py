@@ -305,3 +305,47 @@ def test_plan_balanced_grid(lib, M, N):
     rounds = -(-units // full)
     assert -(-units // clusters) == rounds
     assert clusters == 1 or -(-units // (clusters - 1)) > rounds
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A, None, 0, 64, 0, 0, 0, A, A, None), binding.SVDQ_OK),
+    ((None, None, 0, 64, 8, 0, 0, None, None, None), binding.SVDQ_OK),
+    ((A, None, 40, 64, 0, 0, 0, A, A, None), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    ((A, None, 32, 96, 0, 0, 0, A, A, None), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    ((A, A, 32, 64, 129, 0, 0, A, A, A), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    ((A, None, -16, 64, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, None, 32, 0, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((None, None, 32, 64, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, None, 32, 64, 0, 0, 0, None, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, None, 32, 64, 8, 0, 0, A, A, A), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, A, 32, 64, 8, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, None, 32, 64, 0, 2, 0, A, A, None), binding.SVDQ_ERR_BAD_OPTION),
+    ((A, None, 32, 64, 0, 0, 2, A, A, None), binding.SVDQ_ERR_BAD_OPTION),
+    ((A + 8, None, 32, 64, 0, 0, 0, A, A, None), binding.SVDQ_ERR_MISALIGNED),
+    ((A, A + 2, 32, 64, 8, 0, 0, A, A, A), binding.SVDQ_ERR_MISALIGNED),
+])
+def test_quantize_host_validation(lib, args, expect):
+    # rejected before any device call (the addresses are fake); the one valid
+    # call is empty (M = 0) and launches nothing
+    assert lib.svdq_quantize_act(*args, None) == expect
+
+
+@pytest.mark.parametrize("M,K,R,splits", [(16, 12288, 32, 8), (256, 3072, 32, 8),
+                                          (1024, 3072, 32, 8), (4096, 3072, 32, 4),
+                                          (4096, 12288, 128, 4), (9728, 3072, 16, 2),
+                                          (16384, 3072, 32, 1), (65536, 3072, 128, 1),
+                                          (4096, 64, 32, 1), (4096, 128, 0, 2)])
+def test_quantize_plan(lib, M, K, R, splits):
+    plan = binding.svdq_quantize_query(M, K, R, sm_count=SMS)
+    tiles = -(-M // 128)
+    assert plan["splits"] == splits
+    assert plan["grid"] == tiles * splits
+    # a split never leaves a CTA without K chunks, and the grid fits the SMs when split
+    assert splits <= K // 64 and (splits == 1 or plan["grid"] <= SMS)
+    assert 3 <= plan["stages"] <= 10
+    r16 = -(-R // 16) * 16
+    stage = 128 * 128 + 128 * r16
+    # the cluster's partials reuse the stages
+    assert plan["stages"] * stage >= 128 * (r16 + 4) * 4
+    assert plan["smem_bytes"] >= plan["stages"] * stage
+    assert plan["smem_bytes"] <= 232448
