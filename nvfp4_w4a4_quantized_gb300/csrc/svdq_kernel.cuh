@@ -37,7 +37,7 @@
 //                swizzle).  LoRA ring item (32 ranks): raw fp32 LA rows, 16-bit
 //                LU rows (64-byte swizzle) and wcscale.
 //   warps 1, 14  MMA issuers (one thread each, leader CTA), alternating ring
-//                items and taking turns (a shared-memory turn word keeps the
+//                items and taking turns (a turn barrier per issuer keeps the
 //                items in ring order): tcgen05.mma kind::mxf4nvf4
 //                block_scale.scale_vec::4X for main items, kind::f16 (bf16 or
 //                fp16) for LoRA items, commits that free ring stages / publish

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full(s), 1);                  // the producer's byte count
-      ptx::mbar_init(empty(s), 4 + (lora ? 1 : 0));  // the chunk's four quantiser warps + the MMA commit
+      ptx::mbar_init(empty(s), 16 + (lora ? 1 : 0));  // every quantiser warp + the MMA commit
     }
     ptx::mbar_init(acc_full, 1);
     *abort_flag = 0;
@@ -263,46 +263,58 @@ __global__ void __launch_bounds__(kQThreads, 1)
   } else {
     // ------------------------------------------------------------ quantisers
     const int q = warp & 3;
-    const int h = (warp - 2) >> 2;  // this warp takes chunks h, h + 4, h + 8, ...
+    // This warp quantises chunks h, h + 4, h + 8, ... (four chunks in work at
+    // once).  It still waits on every chunk's full barrier in order and signs
+    // every chunk's release, so it can never fall two phases behind on a
+    // barrier it tracks by parity, whatever the ring depth.
+    const int h = (warp - 2) >> 2;
     const int r = 32 * q + lane;    // row within the tile (= tensor-memory lane)
     const int grow = tile * kQRows + r;
     const bool live = grow < p.M;
     const int sw = r & 7;  // 128-byte swizzle: 16-byte piece j of row r sits at j ^ (r % 8)
     uint8_t* act_row = p.act + static_cast<size_t>(grow) * static_cast<size_t>(p.K / 2);
     bool ok = true;
-    for (int i = h; i < n; i += 4) {
-      const int stage = i % S;
-      if (!warp_wait_bar<false>(full(stage), static_cast<uint32_t>((i / S) & 1), kSiteQuantFull,
-                                ctl)) {
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < n; ++i) {
+      if (!warp_wait_bar<false>(full(stage), phase, kSiteQuantFull, ctl)) {
         ok = false;
         break;
       }
-      const uint8_t* xr = smem + stage * stage_bytes + r * 128;
-      uint32_t codes[8], sb[4];
+      if ((i & 3) == h) {
+        const uint8_t* xr = smem + stage * stage_bytes + r * 128;
+        uint32_t codes[8], sb[4];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint4 a = lds128(xr + (((2 * g) ^ sw) << 4));
-        const uint4 b = lds128(xr + (((2 * g + 1) ^ sw) << 4));
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        sb[g] = quant_group<F16>(w, scale_tab, codes + 2 * g);
-      }
-      // the stage goes back to the producer once every lane has used its
-      // loaded words (a load is complete once its value has been consumed)
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(empty(stage));
-      if (live) {
-        const int c = c_begin + i;
-        uint4* dst = reinterpret_cast<uint4*>(act_row + 32 * c);
-        dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-        dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-        if (p.packed) {
-          reinterpret_cast<uint32_t*>(p.ascales)[static_cast<size_t>(c) * p.M + grow] =
-              sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
-        } else {
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            p.ascales[static_cast<size_t>(4 * c + g) * p.M + grow] = static_cast<uint8_t>(sb[g]);
+        for (int g = 0; g < 4; ++g) {
+          const uint4 a = lds128(xr + (((2 * g) ^ sw) << 4));
+          const uint4 b = lds128(xr + (((2 * g + 1) ^ sw) << 4));
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          sb[g] = quant_group<F16>(w, scale_tab, codes + 2 * g);
         }
+        // the stage goes back to the producer once every lane has used its
+        // loaded words (a load is complete once its value has been consumed)
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(empty(stage));
+        if (live) {
+          const int c = c_begin + i;
+          uint4* dst = reinterpret_cast<uint4*>(act_row + 32 * c);
+          dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+          if (p.packed) {
+            reinterpret_cast<uint32_t*>(p.ascales)[static_cast<size_t>(c) * p.M + grow] =
+                sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
+          } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              p.ascales[static_cast<size_t>(4 * c + g) * p.M + grow] = static_cast<uint8_t>(sb[g]);
+          }
+        }
+      } else if (lane == 0) {
+        ptx::mbar_arrive(empty(stage));
+      }
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
     // every quantiser has finished with the stages (the partials reuse them)
