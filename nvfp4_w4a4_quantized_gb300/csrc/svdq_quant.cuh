@@ -164,15 +164,30 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const Ctl ctl{abort_flag, p.status, p.timeout_ns};
   // E4M3 byte -> 1/value as hi + lo; 0x7F (NaN) is never produced
   float2* scale_tab = reinterpret_cast<float2*>(bar_area + 8 * (2 * kQMaxStages + 1) + 16);
-  if (threadIdx.x < 128) {
-    const float v = threadIdx.x < 0x7F ? ptx::e4m3_value(threadIdx.x) : 0.0f;
+  // built by warps 2..5 while thread 0 starts the ring
+  if (threadIdx.x >= 64 && threadIdx.x < 64 + 128) {
+    const uint32_t b = threadIdx.x - 64;
+    const float v = b < 0x7F ? ptx::e4m3_value(b) : 0.0f;
     const float hi = v > 0.0f ? __frcp_rn(v) : 0.0f;
     // 1 - v hi is exact in one fma (v has 4 significant bits); times hi it is
     // 1/v - hi to fp32 precision
     const float lo = __fmul_rn(__fmaf_rn(-v, hi, 1.0f), hi);
-    scale_tab[threadIdx.x] = make_float2(hi, v > 0.0f ? lo : 0.0f);
+    scale_tab[b] = make_float2(hi, v > 0.0f ? lo : 0.0f);
   }
 
+  // Thread 0 is the producer: it sets up the barriers and issues the ring's
+  // first S loads (every stage starts empty) before the CTA-wide barrier, so
+  // the first chunks are in flight while the rest of the set-up runs.
+  const uint32_t load_bytes = static_cast<uint32_t>(kQXBytes + (lora ? 128 * p.r16 : 0));
+  auto issue = [&](int i) {
+    const int stage = i % S;
+    const uint32_t st = sbase + stage * stage_bytes;
+    const int kx = (c_begin + i) * kQChunk;
+    ptx::mbar_arrive_expect_tx(full(stage), load_bytes);
+    ptx::tma_load_2d(st, &tm_x, full(stage), kx, tile * kQRows);
+    if (lora) ptx::tma_load_2d(st + kQXBytes, &tm_ld, full(stage), kx, 0);
+  };
+  const int pre = n < S ? n : S;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full(s), 1);                  // the producer's byte count
@@ -181,10 +196,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
     ptx::mbar_init(acc_full, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tm_x);
     if (lora) ptx::prefetch_tmap(&tm_ld);
+    // x is read only once the previous kernel of the stream has completed
+    ptx::griddep_wait();
+    for (int i = 0; i < pre; ++i) issue(i);
   }
   if (warp == 1 && lora) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
@@ -202,22 +218,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint32_t bytes = static_cast<uint32_t>(kQXBytes + (lora ? 128 * p.r16 : 0));
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      for (int i = 0; i < n; ++i) {
-        if (!wait_bar<false>(empty(stage), phase ^ 1u, kSiteQuantEmpty, ctl)) break;
-        const uint32_t st = sbase + stage * stage_bytes;
-        const int kx = (c_begin + i) * kQChunk;
-        ptx::mbar_arrive_expect_tx(full(stage), bytes);
-        ptx::tma_load_2d(st, &tm_x, full(stage), kx, tile * kQRows);
-        if (lora) ptx::tma_load_2d(st + kQXBytes, &tm_ld, full(stage), kx, 0);
+      int issued = pre;
+      for (int i = pre; i < n; ++i) {
+        // the stage's previous chunk (i - S) has been released
+        if (!wait_bar<false>(empty(i % S), static_cast<uint32_t>(((i / S) & 1) ^ 1),
+                             kSiteQuantEmpty, ctl))
+          break;
+        issue(i);
         ++issued;
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
-        }
       }
       // every copy this thread started has landed before the CTA can exit
       for (int j = issued > S ? issued - S : 0; j < issued; ++j)
