@@ -30,12 +30,14 @@ timing; the planner decides the split, e.g. on mlp_down_256x3072x12288_r128).
 Calls are bit-reproducible by default (the MMA issuers take turns);
 `--relaxed-order` times svdq_options_t.relaxed_order = 1 instead.
 A default run (no route flag) also records, under `routes`, the prepacked,
-prepacked + packed-scale and relaxed-order routes of the same workload, timed
+prepacked + packed-scale, relaxed-order and quantiser-format (packed scales +
+16-bit LoRA activations, `lora_act_16bit`) routes of the same workload, timed
 the same way (flushed L2, per-launch events, 10 launches each), and under
 `per_shape` every benchmark workload timed the same way: the tiny case, the
 attention projection, MLP-up and MLP-down, each on the default route, the
-dense calibration variant (R = 0, no wcscale / bias) and the prepacked +
-packed-scale route, and the 24-case token-count sweep (default route, plus
+dense calibration variant (R = 0, no wcscale / bias), the prepacked +
+packed-scale route and that route with 16-bit LoRA activations, and the
+24-case token-count sweep (default route, plus
 the split-K entry point where the planner splits); then the activation
 quantiser on the production activations (GB/s against the measured HBM copy
 bandwidth) and the whole layer from 16-bit activations (quantiser with
@@ -356,6 +358,15 @@ def run_per_shape(pkg, synth, torch, dev, stream, flush, fp4_peak):
                                          d["wcscale"], d["bias"], out, stream=stream, options=o2)
         e["prepacked_packed_scales"] = shape_entry(
             float(w.flops), time_flushed(call_pk, flush, stream, 3, 10, torch, dev), fp4_peak)
+        # ... and the quantiser's formats: packed scales and 16-bit LA
+        la16 = d["lora_act_in"].to(torch.bfloat16)
+        o3 = dict(act_scales_packed=1, lora_act_16bit=1)
+
+        def call_q():
+            pkg.svdq_w4a4_gemm_prepacked(d["act"], d["wgt"], apk, wpk, la16, lup, d["wcscale"],
+                                         d["bias"], out, stream=stream, options=o3)
+        e["prepacked_packed_scales_lora16"] = shape_entry(
+            float(w.flops), time_flushed(call_q, flush, stream, 3, 10, torch, dev), fp4_peak)
         res[w.name] = e
         del d, out, wpk, lup, apk
     sweep = []
@@ -444,19 +455,20 @@ def run_quantize_shapes(pkg, synth, torch, dev, stream, flush, fp4_peak):
         a = synth.make_activations(w.M, w.K, w.R, seed=w.seed + 100)
         x, ld = a["x"].to(dev), a["lora_down"].to(dev)
         wpk, lup = pkg.svdq_prepack_weights(d["wscales"], d["lora_up"], d["wcscale"])
-        act, apk, la = pkg.svdq_quantize_act(x, ld, scales_packed=True)
+        act, apk, la = pkg.svdq_quantize_act(x, ld, scales_packed=True, lora_act_16bit=True)
         out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
-        o2 = dict(act_scales_packed=1)
+        o2 = dict(act_scales_packed=1, lora_act_16bit=1)
 
         def call_layer():
-            pkg.svdq_quantize_act(x, ld, act, apk, la, scales_packed=True, stream=stream)
+            pkg.svdq_quantize_act(x, ld, act, apk, la, scales_packed=True, lora_act_16bit=True,
+                                  stream=stream)
             pkg.svdq_w4a4_gemm_prepacked(act, d["wgt"], apk, wpk, la, lup, d["wcscale"],
                                          d["bias"], out, stream=stream, options=o2)
         e = shape_entry(float(w.flops), time_flushed(call_layer, flush, stream, 3, 10, torch,
                                                      dev), fp4_peak)
-        e["how"] = ("svdq_quantize_act (packed scales) + svdq_w4a4_gemm_prepacked "
-                    "(act_scales_packed) in one event pair; tflops counts the operator's "
-                    "2MNK + 2MNR")
+        e["how"] = ("svdq_quantize_act (packed scales, 16-bit LA) + svdq_w4a4_gemm_prepacked "
+                    "(act_scales_packed, lora_act_16bit) in one event pair; tflops counts the "
+                    "operator's 2MNK + 2MNR")
         layer[w.name] = e
         del d, x, ld, wpk, lup, act, apk, la, out
     return {"quantize": quant, "layer_from_16bit_x": layer}
@@ -623,15 +635,22 @@ def run_ours(args, w, rank, world, local_rank):
                                                 d.get("wcscale"))
             apk = pkg.svdq_pack_scales(d["ascales"])
             torch.cuda.synchronize(dev)
-            cases = {"prepacked": (d["ascales"], {}),
-                     "prepacked_packed_scales": (apk, dict(act_scales_packed=1)),
-                     "prepacked_packed_scales_relaxed_order": (apk, dict(act_scales_packed=1,
-                                                                         relaxed_order=1))}
-            for name, (asc, extra) in cases.items():
+            la = d.get("lora_act_in")
+            la16 = la.to(out.dtype) if la is not None and w.R % 8 == 0 else None
+            cases = {"prepacked": (d["ascales"], la, {}),
+                     "prepacked_packed_scales": (apk, la, dict(act_scales_packed=1)),
+                     "prepacked_packed_scales_relaxed_order": (apk, la, dict(act_scales_packed=1,
+                                                                             relaxed_order=1))}
+            if la16 is not None:
+                # the formats the activation quantiser writes: packed scales,
+                # 16-bit LA (64-rank LoRA items)
+                cases["prepacked_packed_scales_lora16"] = (
+                    apk, la16, dict(act_scales_packed=1, lora_act_16bit=1))
+            for name, (asc, la_in, extra) in cases.items():
                 o2 = dict(opts, **extra)
 
                 def call():
-                    pkg.svdq_w4a4_gemm_prepacked(d["act"], d["wgt"], asc, wpk, d.get("lora_act_in"),
+                    pkg.svdq_w4a4_gemm_prepacked(d["act"], d["wgt"], asc, wpk, la_in,
                                                  lup, d.get("wcscale"), d.get("bias"), out,
                                                  stream=stream, options=o2)
                 for _ in range(3):

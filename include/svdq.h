@@ -142,6 +142,16 @@ typedef struct svdq_options {
                             within the stated tolerance) may change from call to
                             call, for a few percent more speed when scales arrive
                             packed                                               */
+    int32_t lora_act_16bit; /* 0 = lora_act_in is fp32 [M, R] (default); 1 = it holds
+                            the 16-bit values [M, R] in the I/O type (bf16, or fp16
+                            with io_dtype fp16; pass the buffer's address cast to
+                            const float*): the LoRA operand the tensor cores take,
+                            which the kernel otherwise rounds from fp32 (RNE), as an
+                            activation quantiser can write it.  The operator then
+                            carries 64 ranks per LoRA ring item instead of 32
+                            (half the ring slots at R = 128).  Needs R a multiple
+                            of 8 (SVDQ_ERR_BAD_OPTION otherwise); results equal
+                            the fp32 route's on the rounded values, bit for bit */
 } svdq_options_t;
 
 /* svdq_w4a4_gemm with options; identical semantics otherwise.  With
@@ -226,9 +236,12 @@ int svdq_pack_scales(const void* scales, int64_t rows, int64_t K, void* packed, 
  * scales_packed 0: ascales is uint8 [K/16, M] (svdq_w4a4_gemm's layout);
  *               1: uint32 [K/64, M] words, word (s, m) byte g = scale of group
  *               4s + g (svdq_pack_scales' layout, for act_scales_packed).
+ * lora_act_16bit 0: lora_act_in is fp32; 1: it is written in x's 16-bit type,
+ *               rounded to nearest even from the fp32 sum (the operand the
+ *               operator's lora_act_16bit option takes).
  * act           device, uint8 [M, K/2]: low nibble = even k.
  * ascales       device, as selected by scales_packed.
- * lora_act_in   device, fp32 [M, R]; NULL iff R == 0.  Accumulated in fp32 on
+ * lora_act_in   device, fp32 (or 16-bit) [M, R]; NULL iff R == 0.  Accumulated in fp32 on
  *               the tensor cores from the 16-bit products; with several CTAs
  *               per 128-row tile their fp32 partials are added in a fixed
  *               order, so the same call gives the same bits every time.
@@ -240,8 +253,8 @@ int svdq_pack_scales(const void* scales, int64_t rows, int64_t K, void* packed, 
  * device status word.
  */
 int svdq_quantize_act(const void* x, const void* lora_down, int64_t M, int64_t K, int64_t R,
-                      int32_t io_dtype, int32_t scales_packed, void* act, void* ascales,
-                      float* lora_act_in, void* stream);
+                      int32_t io_dtype, int32_t scales_packed, int32_t lora_act_16bit, void* act,
+                      void* ascales, void* lora_act_in, void* stream);
 
 /* The launch svdq_quantize_act would make (host only; touches no device when
  * sm_count > 0): CTAs per 128-row tile along K (*splits, 1, 2, 4 or 8: a
@@ -409,7 +422,7 @@ const char* svdq_status_string(int status);
 /* Library ABI version (major * 10000 + minor * 100 + patch).  The structs
  * above grow only at their end; a caller built against a header with another
  * major.minor (SVDQ_ABI_VERSION / 100) must not pass them to this library. */
-#define SVDQ_ABI_VERSION 600
+#define SVDQ_ABI_VERSION 700
 int svdq_version(void);
 
 #ifdef __cplusplus

@@ -15,7 +15,7 @@ from typing import Optional
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsvdq.so")
 # include/svdq.h SVDQ_ABI_VERSION the structs below mirror
-ABI_VERSION = 600
+ABI_VERSION = 700
 # include/svdq.h size limits
 SVDQ_MAX_MN = 1 << 24
 SVDQ_MAX_K = 1 << 20
@@ -52,7 +52,8 @@ class SvdqOptions(ctypes.Structure):
                 ("max_ctas", ctypes.c_int32), ("timeout_ms", ctypes.c_int32),
                 ("debug_fault", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("io_dtype", ctypes.c_int32), ("k_splits", ctypes.c_int32),
-                ("act_scales_packed", ctypes.c_int32), ("relaxed_order", ctypes.c_int32)]
+                ("act_scales_packed", ctypes.c_int32), ("relaxed_order", ctypes.c_int32),
+                ("lora_act_16bit", ctypes.c_int32)]
 
 
 class SvdqPlan(ctypes.Structure):
@@ -129,7 +130,7 @@ def load(path: Optional[str] = None):
         lib.svdq_version.restype = ctypes.c_int
         lib.svdq_version.argtypes = []
         lib.svdq_quantize_act.restype = ctypes.c_int
-        lib.svdq_quantize_act.argtypes = [vp, vp] + [i64] * 3 + [i32] * 2 + [vp] * 4
+        lib.svdq_quantize_act.argtypes = [vp, vp] + [i64] * 3 + [i32] * 3 + [vp] * 4
         lib.svdq_quantize_query.restype = ctypes.c_int
         lib.svdq_quantize_query.argtypes = [i64] * 3 + [i32] + [ctypes.POINTER(i32)] * 4
         # the ctypes structs here mirror include/svdq.h at ABI_VERSION
@@ -240,11 +241,13 @@ def _gemm(act, wgt, ascales, wscales, lora_act_in, lora_up, wcscale, bias, out, 
     ws_dt = torch.int32 if prepacked else torch.uint8
     ws_shape = (K // 64, N) if prepacked else (K // 16, N)
     act_packed = bool(_opts(options) and _opts(options).act_scales_packed)
+    # lora_act_in as 16-bit values in the I/O type (lora_act_16bit) or fp32
+    la_dt = h16 if (_opts(options) and _opts(options).lora_act_16bit) else torch.float32
     as_dt = torch.int32 if act_packed else torch.uint8
     as_shape = (K // 64, M) if act_packed else (K // 16, M)
     for name, t, dt in (("act", act, torch.uint8), ("wgt", wgt, torch.uint8),
                         ("ascales", ascales, as_dt), ("wscales", wscales, ws_dt),
-                        ("lora_act_in", lora_act_in, torch.float32),
+                        ("lora_act_in", lora_act_in, la_dt),
                         ("lora_up", lora_up if R else None, h16), ("wcscale", wcscale, h16),
                         ("bias", bias, h16), ("out", out, h16)):
         if t is not None:
@@ -384,12 +387,14 @@ def svdq_version() -> int:
 
 
 def svdq_quantize_act(x, lora_down=None, act=None, ascales=None, lora_act_in=None,
-                      scales_packed: bool = False, stream=None, check: bool = True):
+                      scales_packed: bool = False, lora_act_16bit: bool = False, stream=None,
+                      check: bool = True):
     """The operator's activation inputs from 16-bit activations x [M, K]
     (bf16 or fp16): returns (act uint8 [M, K/2], ascales uint8 [K/16, M] or
-    int32 words [K/64, M] with ``scales_packed``, lora_act_in fp32 [M, R] or
-    None).  lora_down is [R, K] in x's type, or None for R = 0.  Outputs are
-    allocated here unless given.  Asynchronous on ``stream``."""
+    int32 words [K/64, M] with ``scales_packed``, lora_act_in [M, R] or None:
+    fp32, or x's 16-bit type with ``lora_act_16bit``).  lora_down is [R, K] in
+    x's type, or None for R = 0.  Outputs are allocated here unless given.
+    Asynchronous on ``stream``."""
     import torch
 
     if x.dtype not in (torch.bfloat16, torch.float16):
@@ -407,21 +412,23 @@ def svdq_quantize_act(x, lora_down=None, act=None, ascales=None, lora_act_in=Non
     sc_dt, sc_shape = (torch.int32, (K // 64, M)) if scales_packed else (torch.uint8, (K // 16, M))
     if ascales is None:
         ascales = torch.empty(sc_shape, dtype=sc_dt, device=dev)
+    la_dt = x.dtype if lora_act_16bit else torch.float32
     if R and lora_act_in is None:
-        lora_act_in = torch.empty((M, R), dtype=torch.float32, device=dev)
+        lora_act_in = torch.empty((M, R), dtype=la_dt, device=dev)
     _check("act", act, torch.uint8)
     _check("ascales", ascales, sc_dt)
     if tuple(act.shape) != (M, K // 2) or tuple(ascales.shape) != sc_shape:
         raise ValueError("inconsistent output shapes")
     if R:
-        _check("lora_act_in", lora_act_in, torch.float32)
+        _check("lora_act_in", lora_act_in, la_dt)
         if tuple(lora_act_in.shape) != (M, R):
             raise ValueError("lora_act_in must be [M, R]")
     io = SVDQ_IO_FP16 if x.dtype == torch.float16 else SVDQ_IO_BF16
     h = _stream_handle(stream, dev)
     with torch.cuda.device(dev):
         rc = load().svdq_quantize_act(_ptr(x), _ptr(lora_down) if R else None, M, K, R, io,
-                                      1 if scales_packed else 0, _ptr(act), _ptr(ascales),
+                                      1 if scales_packed else 0, 1 if lora_act_16bit else 0,
+                                      _ptr(act), _ptr(ascales),
                                       _ptr(lora_act_in) if R else None, h)
     if check and rc != SVDQ_OK:
         raise SvdqError(rc, "svdq_quantize_act")

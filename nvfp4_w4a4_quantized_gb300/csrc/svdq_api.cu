@@ -89,6 +89,7 @@ int validate_options(const svdq_options_t* o) {
   if (o->k_splits < -1 || o->k_splits > kMaxSplits) return SVDQ_ERR_BAD_OPTION;
   if (o->act_scales_packed != 0 && o->act_scales_packed != 1) return SVDQ_ERR_BAD_OPTION;
   if (o->relaxed_order != 0 && o->relaxed_order != 1) return SVDQ_ERR_BAD_OPTION;
+  if (o->lora_act_16bit != 0 && o->lora_act_16bit != 1) return SVDQ_ERR_BAD_OPTION;
   return SVDQ_OK;
 }
 
@@ -217,11 +218,15 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t R, const svdq_options_t* 
   pl.acc_stages = ti.acc_stages;
   pl.smem_bytes = ti.fixed_smem + pl.stages * ti.stage_bytes;
   pl.tmem_cols_used = ti.acc_cols + pl.stages * ti.sf_cols;
-  pl.lora_block_bytes = ti.lora_block_bytes;
+  // 16-bit LA': 64-rank items of LA' [128][64] + LU' [tile_n / cg][64] + wcscale
+  const bool la16 = o && o->lora_act_16bit;
+  const int lora_ranks = la16 ? 64 : kLoraRanks;
+  pl.lora_block_bytes =
+      la16 ? kBM * 128 + (pl.tile_n / pl.cta_group) * 130 : ti.lora_block_bytes;
   pl.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
   pl.kbi = ti.kbi;
   pl.main_items = (pl.k_blocks + pl.kbi - 1) / pl.kbi;
-  pl.lora_blocks = static_cast<int>((R + kLoraRanks - 1) / kLoraRanks);
+  pl.lora_blocks = static_cast<int>((R + lora_ranks - 1) / lora_ranks);
   pl.r16 = static_cast<int>((R + 15) / 16 * 16);
   const int tm = kBM * pl.cta_group;
   pl.tiles_m = static_cast<int>((M + tm - 1) / tm);
@@ -435,7 +440,20 @@ int launch(const Plan& pl, DeviceInfo* dinfo, const Operands& op, const KParams&
                      CU_TENSOR_MAP_SWIZZLE_64B)) != SVDQ_OK)
       return rc;
   }
-  if (kp.lora_tma) {
+  if (kp.la16) {
+    // 16-bit LA' and LU: 64 ranks (128 bytes) per box, 128-byte swizzle,
+    // row-quad order like the operand tiles
+    const uint64_t r64 = static_cast<uint64_t>(R);
+    const uint64_t d_la[3] = {r64, M4, 4}, s_la[2] = {8 * r64, 2 * r64};
+    const uint32_t b_lora[3] = {64, 32, 4};
+    if ((rc = encode(&tm[4], kIoType, 3, op.la, d_la, s_la, b_lora,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
+      return rc;
+    const uint64_t d_lu[3] = {r64, N4, 4};
+    if ((rc = encode(&tm[5], kIoType, 3, op.lu, d_lu, s_la, b_lora,
+                     CU_TENSOR_MAP_SWIZZLE_128B)) != SVDQ_OK)
+      return rc;
+  } else if (kp.lora_tma) {
     const uint64_t r64 = static_cast<uint64_t>(R);
     const uint64_t d_la[3] = {r64, M4, 4}, s_la[2] = {16 * r64, 4 * r64};
     const uint32_t b_lora[3] = {kLoraRanks, 32, 4};
@@ -555,6 +573,9 @@ int run_gemm(const void* act, const void* wgt, const void* ascales, const void* 
   if (!act || !wgt || !ascales || !wscales || !out) return SVDQ_ERR_INVALID_ARG;
   if (R > 0 && (!lora_act_in || !lora_up)) return SVDQ_ERR_INVALID_ARG;
   if ((rc = validate_shape(M, N, K, R)) != SVDQ_OK) return rc;
+  const bool la16 = options != nullptr && options->lora_act_16bit && R > 0;
+  // 16-bit LA' rows go through TMA: their stride (2R bytes) must be 16-byte aligned
+  if (la16 && R % 8) return SVDQ_ERR_BAD_OPTION;
   const void* ptrs[] = {act, wgt, ascales, wscales, out, lora_act_in, lora_up, wcscale, bias};
   for (const void* p : ptrs)
     if (p && !aligned(p, 16)) return SVDQ_ERR_MISALIGNED;
@@ -583,6 +604,8 @@ int run_gemm(const void* act, const void* wgt, const void* ascales, const void* 
   kp.r16 = pl.r16;
   kp.num_stages = pl.stages;
   kp.lora_tma = (R > 0 && R % 8 == 0);
+  kp.la16 = la16 ? 1 : 0;
+  kp.lora_ranks = la16 ? 64 : kLoraRanks;
   kp.prepacked = prepacked ? 1 : 0;
   kp.act_packed = (options != nullptr && options->act_scales_packed) ? 1 : 0;
   kp.splits = pl.splits;
@@ -649,8 +672,8 @@ int plan_quant(int64_t M, int64_t K, int64_t R, int sm_count, int smem_optin, Qu
 
 template <bool F16>
 int launch_quant(const QuantPlan& qp, DeviceInfo* dinfo, const void* x, const void* ld,
-                 int64_t M, int64_t K, int64_t R, int packed, void* act, void* ascales,
-                 float* la, cudaStream_t stream) {
+                 int64_t M, int64_t K, int64_t R, int packed, int la16, void* act, void* ascales,
+                 void* la, cudaStream_t stream) {
   constexpr CUtensorMapDataType kIoType =
       F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   auto kern = svdq_quant_kernel<F16>;
@@ -688,6 +711,7 @@ int launch_quant(const QuantPlan& qp, DeviceInfo* dinfo, const void* x, const vo
   p.act = static_cast<uint8_t*>(act);
   p.ascales = static_cast<uint8_t*>(ascales);
   p.la = la;
+  p.la16 = la16;
   p.M = static_cast<int>(M);
   p.K = static_cast<int>(K);
   p.R = static_cast<int>(R);
@@ -722,10 +746,11 @@ int launch_quant(const QuantPlan& qp, DeviceInfo* dinfo, const void* x, const vo
 }
 
 int validate_quant(const void* x, const void* ld, int64_t M, int64_t K, int64_t R,
-                   int32_t io_dtype, int32_t packed, const void* act, const void* ascales,
-                   const float* la) {
+                   int32_t io_dtype, int32_t packed, int32_t la16, const void* act,
+                   const void* ascales, const void* la) {
   if (io_dtype != SVDQ_IO_BF16 && io_dtype != SVDQ_IO_FP16) return SVDQ_ERR_BAD_OPTION;
   if (packed != 0 && packed != 1) return SVDQ_ERR_BAD_OPTION;
+  if (la16 != 0 && la16 != 1) return SVDQ_ERR_BAD_OPTION;
   if (M < 0 || K <= 0 || R < 0) return SVDQ_ERR_INVALID_ARG;
   if (M % 16 || K % 64 || M > SVDQ_MAX_MN || K > SVDQ_MAX_K || R > SVDQ_MAX_RANK)
     return SVDQ_ERR_UNSUPPORTED_SHAPE;
@@ -1015,11 +1040,12 @@ extern "C" int svdq_w4a4_gemm_split_noalloc(const void* act, const void* wgt, co
 }
 
 extern "C" int svdq_quantize_act(const void* x, const void* lora_down, int64_t M, int64_t K,
-                                 int64_t R, int32_t io_dtype, int32_t scales_packed, void* act,
-                                 void* ascales, float* lora_act_in, void* stream) {
+                                 int64_t R, int32_t io_dtype, int32_t scales_packed,
+                                 int32_t lora_act_16bit, void* act, void* ascales,
+                                 void* lora_act_in, void* stream) {
   using namespace svdq;
-  int rc = validate_quant(x, lora_down, M, K, R, io_dtype, scales_packed, act, ascales,
-                          lora_act_in);
+  int rc = validate_quant(x, lora_down, M, K, R, io_dtype, scales_packed, lora_act_16bit, act,
+                          ascales, lora_act_in);
   if (rc != SVDQ_OK) return rc;
   if (M == 0) return SVDQ_OK;
   int dev = 0;
@@ -1029,10 +1055,10 @@ extern "C" int svdq_quantize_act(const void* x, const void* lora_down, int64_t M
   if ((rc = plan_quant(M, K, R, dinfo->sm_count, dinfo->smem_optin, &qp)) != SVDQ_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return io_dtype == SVDQ_IO_FP16
-             ? launch_quant<true>(qp, dinfo, x, lora_down, M, K, R, scales_packed, act, ascales,
-                                  lora_act_in, s)
-             : launch_quant<false>(qp, dinfo, x, lora_down, M, K, R, scales_packed, act, ascales,
-                                   lora_act_in, s);
+             ? launch_quant<true>(qp, dinfo, x, lora_down, M, K, R, scales_packed,
+                                  lora_act_16bit, act, ascales, lora_act_in, s)
+             : launch_quant<false>(qp, dinfo, x, lora_down, M, K, R, scales_packed,
+                                   lora_act_16bit, act, ascales, lora_act_in, s);
 }
 
 extern "C" int svdq_quantize_query(int64_t M, int64_t K, int64_t R, int32_t sm_count,

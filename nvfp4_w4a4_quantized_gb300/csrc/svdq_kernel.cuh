@@ -143,6 +143,11 @@ struct Layout {
   static constexpr int kLoraLU = kLuInA ? kOffA + 8192 : kOffB;
   static constexpr int kLoraRawLA = kLuInA ? kOffB : kOffB + kBNc * 64;
   static constexpr int kLoraWC = kOffSFA;
+  // LoRA item with 16-bit LA' (64 ranks, 128-byte rows, 128-byte swizzle):
+  // LA' [128][64] over the A tile, LU' [kBNc][64] over the B tile (the same sizes)
+  static constexpr int kLora16LA = kOffA;
+  static constexpr int kLora16LU = kOffB;
+  static_assert(kBM * 128 <= kATile && kBNc * 128 <= kBTile, "64-rank LoRA item fits the stage");
   static_assert(kLoraRawLA + kBM * kLoraRanks * 4 <= kOffSFA, "LoRA item fits the stage");
   static_assert(2 * kBNc <= 16 * kBM, "wcscale fits the scale area");
   static constexpr int kAccStages = (BN == 256) ? 1 : 2;
@@ -177,7 +182,9 @@ struct KParams {
   int tiles_m, tiles_n, num_tiles, group_m;
   int k_blocks;     // ceil(K / 256)
   int main_items;   // ceil(k_blocks / K blocks per item)
-  int lora_blocks;  // ceil(R / 32)
+  int lora_blocks;  // ceil(R / lora_ranks)
+  int lora_ranks;   // ranks per LoRA ring item: 32, or 64 with 16-bit LA
+  int la16;         // lora_act_in holds 16-bit LA' [M][R] (TMA'd as is, 64 ranks per item)
   int r16;          // R rounded up to 16
   int num_stages;
   int lora_tma;     // R % 8 == 0: LoRA rows arrive by TMA; else direct loads
@@ -497,6 +504,37 @@ __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* w
   bad_col = any_bad ? n_cta + quad_row(bad_row) : bad_col;
 }
 
+// As lora_lu_scale_smem for the 64-rank item's LU' (128-byte rows, 128-byte
+// swizzle: a row's eight 16-byte chunks stay in the row, so scaling whole
+// rows is layout-independent).
+template <int NR, bool F16>
+__device__ __forceinline__ void lora_lu_scale_smem128(uint8_t* lu, const uint8_t* wc, int n_cta,
+                                                      int N, int r0, int lane, int& zero_col,
+                                                      int& bad_col) {
+  using H = H16<F16>;
+  float inv[NR / 32];
+  lora_inv_wc<NR, F16>(inv, wc, n_cta, N, r0, lane, zero_col);
+  const int pc = lane & 7;
+  uint32_t any_bad = 0u;
+  int bad_row = 0;
+#pragma unroll
+  for (int it = 0; it < NR / 4; ++it) {
+    const int row = r0 + it * 4 + (lane >> 3);
+    const float s = __shfl_sync(0xffffffffu, inv[it / 8], (it % 8) * 4 + (lane >> 3));
+    uint4 x = *reinterpret_cast<uint4*>(lu + row * 128 + 16 * pc);
+    x.x = H::pack(__fmul_rn(H::lo(x.x), s), __fmul_rn(H::hi(x.x), s));
+    x.y = H::pack(__fmul_rn(H::lo(x.y), s), __fmul_rn(H::hi(x.y), s));
+    x.z = H::pack(__fmul_rn(H::lo(x.z), s), __fmul_rn(H::hi(x.z), s));
+    x.w = H::pack(__fmul_rn(H::lo(x.w), s), __fmul_rn(H::hi(x.w), s));
+    const uint32_t b = nonfinite16_bits<F16>(x.x) | nonfinite16_bits<F16>(x.y) |
+                       nonfinite16_bits<F16>(x.z) | nonfinite16_bits<F16>(x.w);
+    any_bad |= b;
+    bad_row = b ? row : bad_row;
+    *reinterpret_cast<uint4*>(lu + row * 128 + 16 * pc) = x;
+  }
+  bad_col = any_bad ? n_cta + quad_row(bad_row) : bad_col;
+}
+
 // Direct-load LoRA operands (used when R is not a multiple of 8, so LoRA rows
 // are not 16-byte strided for TMA): LA' tile row r holds matrix row m_cta +
 // quad_row(r), LU' tile row r column n_cta + quad_row(r); ranks 32*blk ..
@@ -661,7 +699,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the LoRA item stages wcscale only to divide LU by it in place
       const bool stage_wc = p.wcscale != nullptr && !p.prepacked;
       const uint32_t lora_aux_bytes =
-          kBM * kLoraRanks * 4 + L::kBNc * 64 + (stage_wc ? 2 * L::kBNc : 0);
+          p.la16 ? kBM * 128 + L::kBNc * 128 + (stage_wc ? 2 * L::kBNc : 0)
+                 : kBM * kLoraRanks * 4 + L::kBNc * 64 + (stage_wc ? 2 * L::kBNc : 0);
       for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
         const Unit w = unit_of<SK>(p, u);
         const int t = w.tile;
@@ -688,7 +727,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (i < w.lora) {
             if (role == 0) {
-              if (p.lora_tma) {
+              if (p.la16) {
+                // 64 ranks of 16-bit LA' and LU (128-byte swizzle), as they come
+                ptx::mbar_arrive_expect_tx(ab, lora_aux_bytes);
+                ptx::tma_load_3d(st + L::kLora16LA, &tm_la, ab, 64 * i, m_cta / 4, 0);
+#pragma unroll
+                for (int h = 0; h < L::kBNc / 128; ++h)
+                  ptx::tma_load_3d(st + L::kLora16LU + 16384 * h, &tm_lu, ab, 64 * i,
+                                   (n_cta + 128 * h) / 4, 0);
+                if (stage_wc) ptx::tma_load_1d(st + L::kLoraWC, &tm_wc, ab, n_cta);
+              } else if (p.lora_tma) {
                 ptx::mbar_arrive_expect_tx(ab, lora_aux_bytes);
                 ptx::tma_load_3d(st + L::kLoraRawLA, &tm_la, ab, kLoraRanks * i, m_cta / 4, 0);
 #pragma unroll
@@ -818,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool lora_item = i < w.lora;
             int nsteps;  // MMAs of this item
             if (lora_item) {
-              nsteps = min(2, (p.r16 - kLoraRanks * i) / 16);
+              nsteps = min(p.lora_ranks / 16, (p.r16 - p.lora_ranks * i) / 16);
             } else {
               // K=64 steps present in this item (the last K block may be partial)
               nsteps = L::kSteps;
@@ -856,8 +904,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             if (lora_item) {
               for (int s = 0; s < nsteps; ++s) {
-                const uint64_t ad = ptx::desc_kmajor_sw64(st + L::kLoraLA + 32 * s);
-                const uint64_t bd = ptx::desc_kmajor_sw64(st + L::kLoraLU + 32 * s);
+                const uint64_t ad = p.la16 ? ptx::desc_kmajor_sw128(st + L::kLora16LA + 32 * s)
+                                           : ptx::desc_kmajor_sw64(st + L::kLoraLA + 32 * s);
+                const uint64_t bd = p.la16 ? ptx::desc_kmajor_sw128(st + L::kLora16LU + 32 * s)
+                                           : ptx::desc_kmajor_sw64(st + L::kLoraLU + 32 * s);
                 if (CG == 2)
                   ptx::mma_bf16_pair(d_tmem, ad, bd, kIdescLora, 1u);
                 else
@@ -928,7 +978,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // LU' rows [h kBNc/2, (h+1) kBNc/2) (the scale feeders build LA')
           uint8_t* st = smem + stage * L::kStageBytes;
           const int r0 = (warp - 2) * (L::kBNc / 2);
-          if (!p.lora_tma)
+          if (p.la16) {
+            if (p.wcscale != nullptr && !p.prepacked)
+              lora_lu_scale_smem128<L::kBNc / 2, F16>(st + L::kLora16LU, st + L::kLoraWC, n_cta,
+                                                      p.N, r0, lane, zero_col, bad_col);
+          } else if (!p.lora_tma)
             lora_lu_direct<L::kBNc / 2, F16>(st + L::kLoraLU, p,
                                              p.prepacked ? nullptr : p.wcscale, n_cta, i, r0,
                                              lane, zero_col, bad_col);
@@ -1189,7 +1243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (i < w.lora) {
+        if (i < w.lora && p.la16) {
+          // 16-bit LA' arrives ready: nothing to build
+        } else if (i < w.lora) {
           // LoRA item: this warp builds LA' rows [32q, 32q + 32)
           uint8_t* st = smem + stage * L::kStageBytes;
           if (p.lora_tma)

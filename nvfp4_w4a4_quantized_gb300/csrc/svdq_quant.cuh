@@ -51,7 +51,8 @@ enum QuantWaitSite : int {
 struct QParams {
   uint8_t* act;       // [M, K/2]
   uint8_t* ascales;   // [K/16, M] bytes, or uint32 [K/64, M] words when packed
-  float* la;          // [M, R]; null when R == 0
+  void* la;           // [M, R] fp32, or 16-bit (la16) in x's type; null when R == 0
+  int la16;           // lora_act_in as 16-bit values (RNE from the fp32 sum)
   int M, K, R, r16;   // r16 = R rounded up to 16 (0 without LoRA)
   int chunks;         // K / 64
   int splits;         // CTAs per row tile (the cluster size), 1..8
@@ -79,6 +80,35 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Columns col .. col + n - 1 (n = 4 or 1) of lora_act_in row `row`: fp32, or
+// 16-bit (RNE) with la16.  n = 4 needs R % 4 == 0 (8- or 16-byte aligned rows).
+template <bool F16>
+__device__ __forceinline__ void store_la(const QParams& p, int row, int col, float4 v, int n) {
+  const size_t at = static_cast<size_t>(row) * p.R + col;
+  if (p.la16) {
+    uint16_t* dst = static_cast<uint16_t*>(p.la) + at;
+    if (n == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(H16<F16>::pack(v.x, v.y), H16<F16>::pack(v.z, v.w));
+    } else {
+      *dst = static_cast<uint16_t>(H16<F16>::pack(v.x, 0.0f) & 0xFFFFu);
+    }
+  } else {
+    float* dst = static_cast<float*>(p.la) + at;
+    if (n == 4)
+      *reinterpret_cast<float4*>(dst) = v;
+    else
+      *dst = v.x;
+  }
 }
 
 // Largest |x| of 16 values given as eight 16-bit pairs (finite values).
@@ -340,18 +370,20 @@ __global__ void __launch_bounds__(kQThreads, 1)
           ptx::tmem_wait_ld();
           if (p.splits == 1) {
             if (live) {
-              float* dst = p.la + static_cast<size_t>(grow) * p.R + c0;
               if ((p.R & 3) == 0 && c0 + 16 <= p.R) {
-                // rows of R % 4 == 0 floats keep 16-byte alignment
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                  reinterpret_cast<float4*>(dst)[j] =
-                      make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                  store_la<F16>(p, grow, c0 + 4 * j,
+                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]),
+                                            __uint_as_float(v[4 * j + 3])),
+                                4);
               } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                  if (c0 + j < p.R) dst[j] = __uint_as_float(v[j]);
+                  if (c0 + j < p.R)
+                    store_la<F16>(p, grow, c0 + j,
+                                  make_float4(__uint_as_float(v[j]), 0.0f, 0.0f, 0.0f), 1);
               }
             }
           } else {
@@ -381,22 +413,39 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int rows = kQRows / p.splits;
     const int row0 = split * rows;
     const int pitch = quant_part_pitch(p.r16);
-    for (int e = static_cast<int>(threadIdx.x); e < rows * p.R; e += kQThreads) {
-      const int rr = row0 + e / p.R;
-      const int col = e % p.R;
+    // four consecutive ranks per thread when rows stay aligned (R % 4 == 0), else one
+    const int vec = (p.R & 3) == 0 ? 4 : 1;
+    const int per_row = p.R / vec;
+    for (int e = static_cast<int>(threadIdx.x); e < rows * per_row; e += kQThreads) {
+      const int rr = row0 + e / per_row;
+      const int col = vec * (e % per_row);
       const uint32_t a = part_base + 4u * static_cast<uint32_t>(rr * pitch + col);
       // all loads first (one distributed-shared-memory latency), then the
       // sum in rank order
-      float part[kQMaxSplits];
+      float4 part[kQMaxSplits];
 #pragma unroll
-      for (int s = 0; s < kQMaxSplits; ++s)
-        part[s] = s < p.splits ? ld_cluster_f32(ptx::mapa(a, static_cast<uint32_t>(s))) : 0.0f;
-      float acc = part[0];
+      for (int s = 0; s < kQMaxSplits; ++s) {
+        part[s] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (s < p.splits) {
+          const uint32_t ra = ptx::mapa(a, static_cast<uint32_t>(s));
+          if (vec == 4)
+            part[s] = ld_cluster_f32x4(ra);
+          else
+            part[s].x = ld_cluster_f32(ra);
+        }
+      }
+      float4 acc = part[0];
 #pragma unroll
-      for (int s = 1; s < kQMaxSplits; ++s)
-        if (s < p.splits) acc += part[s];
+      for (int s = 1; s < kQMaxSplits; ++s) {
+        if (s < p.splits) {
+          acc.x += part[s].x;
+          acc.y += part[s].y;
+          acc.z += part[s].z;
+          acc.w += part[s].w;
+        }
+      }
       const int grow = tile * kQRows + rr;
-      if (grow < p.M) p.la[static_cast<size_t>(grow) * p.R + col] = acc;
+      if (grow < p.M) store_la<F16>(p, grow, col, acc, vec);
     }
     // no CTA leaves while a peer may still read its partials
     __syncwarp();

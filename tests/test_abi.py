@@ -308,21 +308,22 @@ def test_plan_balanced_grid(lib, M, N):
 
 
 @pytest.mark.parametrize("args,expect", [
-    ((A, None, 0, 64, 0, 0, 0, A, A, None), binding.SVDQ_OK),
-    ((None, None, 0, 64, 8, 0, 0, None, None, None), binding.SVDQ_OK),
-    ((A, None, 40, 64, 0, 0, 0, A, A, None), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
-    ((A, None, 32, 96, 0, 0, 0, A, A, None), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
-    ((A, A, 32, 64, 129, 0, 0, A, A, A), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
-    ((A, None, -16, 64, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
-    ((A, None, 32, 0, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
-    ((None, None, 32, 64, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
-    ((A, None, 32, 64, 0, 0, 0, None, A, None), binding.SVDQ_ERR_INVALID_ARG),
-    ((A, None, 32, 64, 8, 0, 0, A, A, A), binding.SVDQ_ERR_INVALID_ARG),
-    ((A, A, 32, 64, 8, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
-    ((A, None, 32, 64, 0, 2, 0, A, A, None), binding.SVDQ_ERR_BAD_OPTION),
-    ((A, None, 32, 64, 0, 0, 2, A, A, None), binding.SVDQ_ERR_BAD_OPTION),
-    ((A + 8, None, 32, 64, 0, 0, 0, A, A, None), binding.SVDQ_ERR_MISALIGNED),
-    ((A, A + 2, 32, 64, 8, 0, 0, A, A, A), binding.SVDQ_ERR_MISALIGNED),
+    ((A, None, 0, 64, 0, 0, 0, 0, A, A, None), binding.SVDQ_OK),
+    ((None, None, 0, 64, 8, 0, 0, 0, None, None, None), binding.SVDQ_OK),
+    ((A, None, 40, 64, 0, 0, 0, 0, A, A, None), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    ((A, None, 32, 96, 0, 0, 0, 0, A, A, None), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    ((A, A, 32, 64, 129, 0, 0, 0, A, A, A), binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    ((A, None, -16, 64, 0, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, None, 32, 0, 0, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((None, None, 32, 64, 0, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, None, 32, 64, 0, 0, 0, 0, None, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, None, 32, 64, 8, 0, 0, 0, A, A, A), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, A, 32, 64, 8, 0, 0, 0, A, A, None), binding.SVDQ_ERR_INVALID_ARG),
+    ((A, None, 32, 64, 0, 2, 0, 0, A, A, None), binding.SVDQ_ERR_BAD_OPTION),
+    ((A, None, 32, 64, 0, 0, 2, 0, A, A, None), binding.SVDQ_ERR_BAD_OPTION),
+    ((A, None, 32, 64, 0, 0, 0, 2, A, A, None), binding.SVDQ_ERR_BAD_OPTION),
+    ((A + 8, None, 32, 64, 0, 0, 0, 0, A, A, None), binding.SVDQ_ERR_MISALIGNED),
+    ((A, A + 2, 32, 64, 8, 0, 0, 0, A, A, A), binding.SVDQ_ERR_MISALIGNED),
 ])
 def test_quantize_host_validation(lib, args, expect):
     # rejected before any device call (the addresses are fake); the one valid

@@ -3,9 +3,9 @@ ABI, against the CPU oracle.
 
 The operator: M, N, K, R and every route drawn at random -- tile and CTA
 group, ring depth, grid cap, per-call or prepacked weights, raw or packed
-activation scales, split-K with the planner's or a forced split count,
-bit-reproducible or relaxed issue order, bf16 or fp16 I/O, wcscale / bias
-present or absent -- checked on sampled rows (every 128-row tile edge and
+activation scales, 16-bit or fp32 LoRA activations, split-K with the
+planner's or a forced split count, bit-reproducible or relaxed issue order,
+bf16 or fp16 I/O, wcscale / bias present or absent -- checked on sampled rows (every 128-row tile edge and
 lane quadrant plus random rows) under the acceptance bound.  The activation
 quantiser: random M, K, R, input type and scale layout, codes and scales bit
 for bit, lora_act_in within its fp32 bound.  Each case is independent; a
@@ -57,12 +57,13 @@ def _gemm_case(seed):
     packed_act = bool(rng.random() < 0.3)
     affine = str(rng.choice(["both", "none", "wc_only", "bias_only"]))
     forced_split = int(rng.integers(2, 5)) if route == "split" and rng.random() < 0.5 else -1
-    return M, N, K, R, half, opts, route, packed_act, affine, forced_split
+    la16 = bool(R % 8 == 0 and R > 0 and rng.random() < 0.4)
+    return M, N, K, R, half, opts, route, packed_act, affine, forced_split, la16
 
 
 @pytest.mark.parametrize("seed", range(GEMM_CASES))
 def test_operator_random_shapes_and_routes(seed):
-    M, N, K, R, half, opts, route, packed_act, affine, forced_split = _gemm_case(seed)
+    M, N, K, R, half, opts, route, packed_act, affine, forced_split, la16 = _gemm_case(seed)
     if route == "split":
         # a forced split needs a K block per part
         if forced_split > 0 and forced_split > -(-K // 256):
@@ -93,15 +94,22 @@ def test_operator_random_shapes_and_routes(seed):
     if R == 0:
         inp["lora_act_in"] = None
         inp["lora_up"] = None
+    h16 = torch.float16 if half else torch.bfloat16
+    if la16:
+        # 16-bit LoRA activations: the oracle sees the same (rounded) values
+        inp["lora_act_in"] = inp["lora_act_in"].to(h16).to(torch.float32)
     d = prepack_gpu(inp, R) if route == "prepacked" or (route == "split" and seed % 2) \
         else to_device(inp)
     prepacked = route == "prepacked" or (route == "split" and seed % 2 == 1)
     if packed_act:
         d["ascales"] = binding.svdq_pack_scales(d["ascales"])
         opts["act_scales_packed"] = 1
-    out = torch.full((M, N), float("nan"), dtype=torch.float16 if half else torch.bfloat16,
-                     device="cuda")
-    args = (d["act"], d["wgt"], d["ascales"], d["wscales"], d["lora_act_in"] if R else None,
+    la_in = d["lora_act_in"] if R else None
+    if la16:
+        opts["lora_act_16bit"] = 1
+        la_in = la_in.to(h16)
+    out = torch.full((M, N), float("nan"), dtype=h16, device="cuda")
+    args = (d["act"], d["wgt"], d["ascales"], d["wscales"], la_in,
             d["lora_up"] if R else None, d.get("wcscale"), d.get("bias"), out)
     if route == "split":
         nbytes = binding.svdq_workspace_size(M, N, K, R, options=opts)

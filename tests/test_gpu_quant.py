@@ -150,11 +150,11 @@ def test_empty_and_rejected_calls():
     xb = torch.zeros(16, 64, dtype=torch.bfloat16, device="cuda")
     out = torch.zeros(16 * 64, dtype=torch.uint8, device="cuda")
     h = torch.cuda.current_stream().cuda_stream
-    assert lib.svdq_quantize_act(xb.data_ptr(), None, 16, 64, 0, 0, 0, out.data_ptr(),
+    assert lib.svdq_quantize_act(xb.data_ptr(), None, 16, 64, 0, 0, 0, 0, out.data_ptr(),
                                  out.data_ptr() + 1, None, h) == binding.SVDQ_ERR_MISALIGNED
-    assert lib.svdq_quantize_act(xb.data_ptr(), None, 16, 64, 4, 0, 0, out.data_ptr(),
+    assert lib.svdq_quantize_act(xb.data_ptr(), None, 16, 64, 4, 0, 0, 0, out.data_ptr(),
                                  out.data_ptr(), None, h) == binding.SVDQ_ERR_INVALID_ARG
-    assert lib.svdq_quantize_act(xb.data_ptr(), None, 8, 64, 0, 0, 0, out.data_ptr(),
+    assert lib.svdq_quantize_act(xb.data_ptr(), None, 8, 64, 0, 0, 0, 0, out.data_ptr(),
                                  out.data_ptr(), None, h) == binding.SVDQ_ERR_UNSUPPORTED_SHAPE
 
 
@@ -180,3 +180,20 @@ def test_quantise_then_gemm(packed):
     inp = dict(w, act=torch.from_numpy(ref_act), ascales=torch.from_numpy(ref_asc),
                lora_act_in=torch.from_numpy(ref_la))
     parity(out.double().cpu().numpy(), oracle_y(inp, M, N, K, R))
+
+
+@pytest.mark.parametrize("half", [False, True], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("M,K,R", [(272, 640, 20), (4096, 3072, 32), (2432, 1024, 128),
+                                   (19456, 128, 64)])
+def test_lora_act_16bit_is_the_rounded_fp32_result(M, K, R, half):
+    # the 16-bit LoRA-down output is the fp32 output rounded to nearest even
+    # (same sum, same order: one CTA per tile and every cluster split)
+    d = synth.make_activations(M, K, R, 50 + R, half=half)
+    x, ld = d["x"].cuda(), d["lora_down"].cuda()
+    _, _, la32 = binding.svdq_quantize_act(x, ld)
+    _, _, la16 = binding.svdq_quantize_act(x, ld, lora_act_16bit=True)
+    torch.cuda.synchronize()
+    code, site, _ = binding.svdq_read_device_status(clear=True)
+    assert code == 0, (code, site)
+    assert la16.dtype == x.dtype
+    assert torch.equal(la16, la32.to(x.dtype))
