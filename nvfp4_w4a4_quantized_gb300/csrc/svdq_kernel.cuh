@@ -453,44 +453,48 @@ __device__ __forceinline__ void lora_la_from_smem(uint8_t* dst, const uint8_t* r
   }
 }
 
-// 1/wcscale for tile rows r0 + lane + 32t (t < NR/32), 0 outside N or for a
-// zero wcscale (fp32 reciprocal, correctly rounded).  zero_col: a column
-// inside N with a zero wcscale, else unchanged (-1).
-template <int NR, bool F16>
-__device__ __forceinline__ void lora_inv_wc(float* inv, const uint8_t* wc, int n_cta, int N,
-                                            int r0, int lane, int& zero_col) {
-#pragma unroll
-  for (int t = 0; t < NR / 32; ++t) {
-    const int off = quad_row(r0 + lane + 32 * t);
-    const float w = H16<F16>::one(*reinterpret_cast<const uint16_t*>(wc + 2 * off));
-    const bool in = n_cta + off < N;
-    inv[t] = (in && w != 0.f) ? __frcp_rn(w) : 0.f;
-    zero_col = (in && w == 0.f) ? n_cta + off : zero_col;
-  }
-}
-
-// LU' rows r0 .. r0+NR-1 in place: every 16-byte chunk of tile row r (column
-// n = n_cta + quad_row(r)) times 1/wcscale[n] (fp32 product, bf16 RNE); the
-// staged wcscale is in plain column order.  Rows outside N (zero-filled) stay
-// zero.  Each row's reciprocal is computed once and shuffled to the row's
-// four lanes.  zero_col / bad_col (-1 if none): a column with a zero wcscale,
-// a column whose LU' is not finite; the caller reports them once its ring
-// arrival is made (the checks are branch-free, off the ring's path).
-template <int NR, bool F16>
-__device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* wc, int n_cta,
-                                                   int N, int r0, int lane, int& zero_col,
-                                                   int& bad_col) {
+// LU' rows [r0, r0 + NR) of a LoRA item in place: tile row r (column n =
+// n_cta + quad_row(r)) times 1/wcscale[n] (fp32 product, 16-bit RNE); the
+// staged wcscale is in plain column order.  ROWB-byte rows: 64 (32 ranks,
+// 64-byte swizzle) or 128 (64 ranks, 128-byte swizzle); a row's 16-byte chunks
+// stay in the row, so whole rows scale alike whatever the swizzle.  Rows
+// outside N (zero-filled) stay zero.  inv[t] holds the reciprocal of row
+// r0 + lane + 32t (0 beyond NR, outside N or for a zero wcscale); it is
+// computed on a tile's first LoRA item (`fresh`) and kept for the others,
+// which carry the same columns.  zero_col / bad_col (-1 if none): a column
+// with a zero wcscale (reported on the fresh item), a column whose LU' is not
+// finite; the caller reports them once its ring arrival is made (the checks
+// are branch-free, off the ring's path).
+template <int NR, int ROWB, bool F16>
+__device__ __forceinline__ void lora_lu_scale(uint8_t* lu, const uint8_t* wc, int n_cta, int N,
+                                              int r0, int lane, bool fresh, float* inv,
+                                              int& zero_col, int& bad_col) {
   using H = H16<F16>;
-  float inv[NR / 32];
-  lora_inv_wc<NR, F16>(inv, wc, n_cta, N, r0, lane, zero_col);
-  const int pc = lane & 3;
+  constexpr int kCpr = ROWB / 16;  // 16-byte chunks per row
+  constexpr int kRpi = 32 / kCpr;  // rows per pass of the warp
+  static_assert(NR % kRpi == 0, "whole passes");
+  if (fresh) {
+#pragma unroll
+    for (int t = 0; t < (NR + 31) / 32; ++t) {
+      const int rl = lane + 32 * t;
+      const int off = quad_row(r0 + rl);
+      const bool mine = rl < NR;
+      const float w = mine ? H::one(*reinterpret_cast<const uint16_t*>(wc + 2 * off)) : 0.f;
+      const bool in = mine && n_cta + off < N;
+      inv[t] = (in && w != 0.f) ? __frcp_rn(w) : 0.f;
+      zero_col = (in && w == 0.f) ? n_cta + off : zero_col;
+    }
+  }
+  const int pc = lane % kCpr;
   uint32_t any_bad = 0u;
   int bad_row = 0;
 #pragma unroll
-  for (int it = 0; it < NR / 8; ++it) {
-    const int row = r0 + it * 8 + (lane >> 2);
-    const float s = __shfl_sync(0xffffffffu, inv[it / 4], (it % 4) * 8 + (lane >> 2));
-    uint4 x = *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc);
+  for (int it = 0; it < NR / kRpi; ++it) {
+    const int rl = it * kRpi + lane / kCpr;
+    const int row = r0 + rl;
+    // rows of one pass share a 32-row block of inv
+    const float s = __shfl_sync(0xffffffffu, inv[(it * kRpi) / 32], rl % 32);
+    uint4 x = *reinterpret_cast<uint4*>(lu + row * ROWB + 16 * pc);
     x.x = H::pack(__fmul_rn(H::lo(x.x), s), __fmul_rn(H::hi(x.x), s));
     x.y = H::pack(__fmul_rn(H::lo(x.y), s), __fmul_rn(H::hi(x.y), s));
     x.z = H::pack(__fmul_rn(H::lo(x.z), s), __fmul_rn(H::hi(x.z), s));
@@ -499,38 +503,7 @@ __device__ __forceinline__ void lora_lu_scale_smem(uint8_t* lu, const uint8_t* w
                        nonfinite16_bits<F16>(x.z) | nonfinite16_bits<F16>(x.w);
     any_bad |= b;
     bad_row = b ? row : bad_row;
-    *reinterpret_cast<uint4*>(lu + row * 64 + 16 * pc) = x;
-  }
-  bad_col = any_bad ? n_cta + quad_row(bad_row) : bad_col;
-}
-
-// As lora_lu_scale_smem for the 64-rank item's LU' (128-byte rows, 128-byte
-// swizzle: a row's eight 16-byte chunks stay in the row, so scaling whole
-// rows is layout-independent).
-template <int NR, bool F16>
-__device__ __forceinline__ void lora_lu_scale_smem128(uint8_t* lu, const uint8_t* wc, int n_cta,
-                                                      int N, int r0, int lane, int& zero_col,
-                                                      int& bad_col) {
-  using H = H16<F16>;
-  float inv[NR / 32];
-  lora_inv_wc<NR, F16>(inv, wc, n_cta, N, r0, lane, zero_col);
-  const int pc = lane & 7;
-  uint32_t any_bad = 0u;
-  int bad_row = 0;
-#pragma unroll
-  for (int it = 0; it < NR / 4; ++it) {
-    const int row = r0 + it * 4 + (lane >> 3);
-    const float s = __shfl_sync(0xffffffffu, inv[it / 8], (it % 8) * 4 + (lane >> 3));
-    uint4 x = *reinterpret_cast<uint4*>(lu + row * 128 + 16 * pc);
-    x.x = H::pack(__fmul_rn(H::lo(x.x), s), __fmul_rn(H::hi(x.x), s));
-    x.y = H::pack(__fmul_rn(H::lo(x.y), s), __fmul_rn(H::hi(x.y), s));
-    x.z = H::pack(__fmul_rn(H::lo(x.z), s), __fmul_rn(H::hi(x.z), s));
-    x.w = H::pack(__fmul_rn(H::lo(x.w), s), __fmul_rn(H::hi(x.w), s));
-    const uint32_t b = nonfinite16_bits<F16>(x.x) | nonfinite16_bits<F16>(x.y) |
-                       nonfinite16_bits<F16>(x.z) | nonfinite16_bits<F16>(x.w);
-    any_bad |= b;
-    bad_row = b ? row : bad_row;
-    *reinterpret_cast<uint4*>(lu + row * 128 + 16 * pc) = x;
+    *reinterpret_cast<uint4*>(lu + row * ROWB + 16 * pc) = x;
   }
   bad_col = any_bad ? n_cta + quad_row(bad_row) : bad_col;
 }
@@ -957,6 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < 4) {
     // ------------------------------------------------------------ LoRA operand builders
+    constexpr int kLuRowsB = L::kBNc / 4;  // LU' rows scaled per builder warp
+    float lu_inv[(kLuRowsB + 31) / 32];
     int stage = 0;
     uint32_t phase = 0;
     const uint32_t full_bar0 = to_leader(full(0));
@@ -975,20 +950,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int zero_col = -1, bad_col = -1;
         if (i < w.lora) {
-          // LU' rows [h kBNc/2, (h+1) kBNc/2) (the scale feeders build LA')
           uint8_t* st = smem + stage * L::kStageBytes;
-          const int r0 = (warp - 2) * (L::kBNc / 2);
-          if (p.la16) {
-            if (p.wcscale != nullptr && !p.prepacked)
-              lora_lu_scale_smem128<L::kBNc / 2, F16>(st + L::kLora16LU, st + L::kLoraWC, n_cta,
-                                                      p.N, r0, lane, zero_col, bad_col);
-          } else if (!p.lora_tma)
+          if (!p.lora_tma && !p.la16) {
+            // direct loads (R not a multiple of 8): LU' rows [h kBNc/2, (h+1) kBNc/2)
             lora_lu_direct<L::kBNc / 2, F16>(st + L::kLoraLU, p,
-                                             p.prepacked ? nullptr : p.wcscale, n_cta, i, r0,
-                                             lane, zero_col, bad_col);
-          else if (p.wcscale != nullptr && !p.prepacked)
-            lora_lu_scale_smem<L::kBNc / 2, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N,
-                                                 r0, lane, zero_col, bad_col);
+                                             p.prepacked ? nullptr : p.wcscale, n_cta, i,
+                                             (warp - 2) * (L::kBNc / 2), lane, zero_col, bad_col);
+          } else if (p.wcscale != nullptr && !p.prepacked) {
+            // LU / wcscale in place: rows [0, kBNc/2) here (a quarter each), the
+            // rest by the scale feeders
+            const int r0 = (warp - 2) * kLuRowsB;
+            if (p.la16)
+              lora_lu_scale<kLuRowsB, 128, F16>(st + L::kLora16LU, st + L::kLoraWC, n_cta, p.N,
+                                                r0, lane, i == 0, lu_inv, zero_col, bad_col);
+            else
+              lora_lu_scale<kLuRowsB, 64, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, r0,
+                                               lane, i == 0, lu_inv, zero_col, bad_col);
+          }
           ptx::fence_proxy_async_smem();
         }
         __syncwarp();
@@ -1226,6 +1204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 12) {
     // ------------------------------------------------------------ scale feeders
     const int q = warp & 3;
+    constexpr int kLuRowsF = L::kBNc / 8;  // LU' rows scaled per feeder warp
+    float lu_inv[(kLuRowsF + 31) / 32];
     int stage = 0;
     uint32_t phase = 0;
     const uint32_t full_bar0 = to_leader(full(0));
@@ -1237,21 +1217,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
+      const int n_cta = nb * BN + L::kBNc * static_cast<int>(rank);
       bool ok = true;
       for (int i = 0; i < n_items; ++i) {
         if (!warp_wait_bar<false>(auxfull(stage), phase, kSiteSfAuxFull, ctl)) {
           ok = false;
           break;
         }
-        if (i < w.lora && p.la16) {
-          // 16-bit LA' arrives ready: nothing to build
-        } else if (i < w.lora) {
-          // LoRA item: this warp builds LA' rows [32q, 32q + 32)
+        int zero_col = -1, bad_col = -1;
+        if (i < w.lora) {
+          // LoRA item: this warp builds LA' rows [32q, 32q + 32) (16-bit LA'
+          // arrives ready) and scales its share of LU' (rows kBNc/2 + q kBNc/8 ..)
           uint8_t* st = smem + stage * L::kStageBytes;
-          if (p.lora_tma)
-            lora_la_from_smem<F16>(st + L::kLoraLA, st + L::kLoraRawLA, 32 * q, lane);
-          else
-            lora_la_direct<32, F16>(st + L::kLoraLA, p, m_cta, i, 32 * q, lane);
+          if (!p.la16) {
+            if (p.lora_tma)
+              lora_la_from_smem<F16>(st + L::kLoraLA, st + L::kLoraRawLA, 32 * q, lane);
+            else
+              lora_la_direct<32, F16>(st + L::kLoraLA, p, m_cta, i, 32 * q, lane);
+          }
+          if ((p.lora_tma || p.la16) && p.wcscale != nullptr && !p.prepacked) {
+            const int r0 = L::kBNc / 2 + q * kLuRowsF;
+            if (p.la16)
+              lora_lu_scale<kLuRowsF, 128, F16>(st + L::kLora16LU, st + L::kLoraWC, n_cta, p.N,
+                                                r0, lane, i == 0, lu_inv, zero_col, bad_col);
+            else
+              lora_lu_scale<kLuRowsF, 64, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, r0,
+                                               lane, i == 0, lu_inv, zero_col, bad_col);
+          }
           ptx::fence_proxy_async_smem();
         } else {
           const uint8_t* st = smem + stage * L::kStageBytes;
@@ -1333,6 +1325,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // leader's MMA reads: the proxy fence above orders them before this
         // arrival (CTA-scope release, as for every other arrival here).
         if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
+        // LoRA operands the accumulator cannot carry (this warp's LU' rows),
+        // reported after the arrival
+        if (i < w.lora) {
+          warp_report_lora(p.status, kStatusWcscaleZero, zero_col >= 0, zero_col);
+          warp_report_lora(p.status, kStatusLuOverflow, bad_col >= 0, bad_col);
+        }
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
