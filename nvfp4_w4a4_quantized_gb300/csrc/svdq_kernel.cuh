@@ -930,45 +930,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < 4) {
     // ------------------------------------------------------------ LoRA operand builders
+    // A unit's LoRA items come first, then its K-block items (nothing to build)
     constexpr int kLuRowsB = L::kBNc / 4;  // LU' rows scaled per builder warp
-    float lu_inv[(kLuRowsB + 31) / 32];
     int stage = 0;
     uint32_t phase = 0;
     const uint32_t full_bar0 = to_leader(full(0));
-    for (int u = cluster_id; u < p.num_units; u += num_clusters) {
+    bool ok = true;
+    for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
       const Unit w = unit_of<SK>(p, u);
       const int t = w.tile;
-      const int n_items = w.lora + w.nkb;
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int n_cta = nb * BN + L::kBNc * static_cast<int>(rank);
-      bool ok = true;
-      for (int i = 0; i < n_items; ++i) {
+      float lu_inv[(kLuRowsB + 31) / 32];
+      for (int i = 0; i < w.lora; ++i) {
         if (!warp_wait_bar<false>(auxfull(stage), phase, kSiteLoraAuxFull, ctl)) {
           ok = false;
           break;
         }
         int zero_col = -1, bad_col = -1;
-        if (i < w.lora) {
-          uint8_t* st = smem + stage * L::kStageBytes;
-          if (!p.lora_tma && !p.la16) {
-            // direct loads (R not a multiple of 8): LU' rows [h kBNc/2, (h+1) kBNc/2)
-            lora_lu_direct<L::kBNc / 2, F16>(st + L::kLoraLU, p,
-                                             p.prepacked ? nullptr : p.wcscale, n_cta, i,
-                                             (warp - 2) * (L::kBNc / 2), lane, zero_col, bad_col);
-          } else if (p.wcscale != nullptr && !p.prepacked) {
-            // LU / wcscale in place: rows [0, kBNc/2) here (a quarter each), the
-            // rest by the scale feeders
-            const int r0 = (warp - 2) * kLuRowsB;
-            if (p.la16)
-              lora_lu_scale<kLuRowsB, 128, F16>(st + L::kLora16LU, st + L::kLoraWC, n_cta, p.N,
-                                                r0, lane, i == 0, lu_inv, zero_col, bad_col);
-            else
-              lora_lu_scale<kLuRowsB, 64, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, r0,
-                                               lane, i == 0, lu_inv, zero_col, bad_col);
-          }
-          ptx::fence_proxy_async_smem();
+        uint8_t* st = smem + stage * L::kStageBytes;
+        if (!p.lora_tma && !p.la16) {
+          // direct loads (R not a multiple of 8): LU' rows [h kBNc/2, (h+1) kBNc/2)
+          lora_lu_direct<L::kBNc / 2, F16>(st + L::kLoraLU, p,
+                                           p.prepacked ? nullptr : p.wcscale, n_cta, i,
+                                           (warp - 2) * (L::kBNc / 2), lane, zero_col, bad_col);
+        } else if (p.wcscale != nullptr && !p.prepacked) {
+          // LU / wcscale in place: rows [0, kBNc/2) here (a quarter each), the
+          // rest by the scale feeders
+          const int r0 = (warp - 2) * kLuRowsB;
+          if (p.la16)
+            lora_lu_scale<kLuRowsB, 128, F16>(st + L::kLora16LU, st + L::kLoraWC, n_cta, p.N,
+                                              r0, lane, i == 0, lu_inv, zero_col, bad_col);
+          else
+            lora_lu_scale<kLuRowsB, 64, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, r0,
+                                             lane, i == 0, lu_inv, zero_col, bad_col);
         }
+        ptx::fence_proxy_async_smem();
         __syncwarp();
         // The pair peer's LoRA rows are generic shared-memory writes that the
         // leader's MMA reads: the proxy fence above orders them before this
@@ -976,16 +974,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
         // LoRA operands the accumulator cannot carry, reported after the
         // arrival so that the ring does not wait for it
-        if (i < w.lora) {
-          warp_report_lora(p.status, kStatusWcscaleZero, zero_col >= 0, zero_col);
-          warp_report_lora(p.status, kStatusLuOverflow, bad_col >= 0, bad_col);
-        }
+        warp_report_lora(p.status, kStatusWcscaleZero, zero_col >= 0, zero_col);
+        warp_report_lora(p.status, kStatusLuOverflow, bad_col >= 0, bad_col);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (!ok) break;
+      for (int j = 0; ok && j < w.nkb; ++j) {
+        if (!warp_wait_bar<false>(auxfull(stage), phase, kSiteLoraAuxFull, ctl)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
     }
   } else if (warp < 8 || warp >= 15) {
     // ------------------------------------------------------------ epilogue
@@ -1203,49 +1209,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < 12) {
     // ------------------------------------------------------------ scale feeders
+    // A unit's LoRA items come first, then its K-block items: two loops, so
+    // the scale feed of the K-block items is compiled on its own.
     const int q = warp & 3;
     constexpr int kLuRowsF = L::kBNc / 8;  // LU' rows scaled per feeder warp
-    float lu_inv[(kLuRowsF + 31) / 32];
     int stage = 0;
     uint32_t phase = 0;
     const uint32_t full_bar0 = to_leader(full(0));
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-    for (int u = cluster_id; u < p.num_units; u += num_clusters) {
+    bool ok = true;
+    for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
       const Unit w = unit_of<SK>(p, u);
       const int t = w.tile;
-      const int n_items = w.lora + w.nkb;
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int m_cta = mb * kBM * CG + kBM * static_cast<int>(rank);
       const int n_cta = nb * BN + L::kBNc * static_cast<int>(rank);
-      bool ok = true;
-      for (int i = 0; i < n_items; ++i) {
+      float lu_inv[(kLuRowsF + 31) / 32];
+      for (int i = 0; i < w.lora; ++i) {
         if (!warp_wait_bar<false>(auxfull(stage), phase, kSiteSfAuxFull, ctl)) {
           ok = false;
           break;
         }
+        // LoRA item: this warp builds LA' rows [32q, 32q + 32) (16-bit LA'
+        // arrives ready) and scales its share of LU' (rows kBNc/2 + q kBNc/8 ..)
         int zero_col = -1, bad_col = -1;
-        if (i < w.lora) {
-          // LoRA item: this warp builds LA' rows [32q, 32q + 32) (16-bit LA'
-          // arrives ready) and scales its share of LU' (rows kBNc/2 + q kBNc/8 ..)
-          uint8_t* st = smem + stage * L::kStageBytes;
-          if (!p.la16) {
-            if (p.lora_tma)
-              lora_la_from_smem<F16>(st + L::kLoraLA, st + L::kLoraRawLA, 32 * q, lane);
-            else
-              lora_la_direct<32, F16>(st + L::kLoraLA, p, m_cta, i, 32 * q, lane);
+        uint8_t* st = smem + stage * L::kStageBytes;
+        if (!p.la16) {
+          if (p.lora_tma)
+            lora_la_from_smem<F16>(st + L::kLoraLA, st + L::kLoraRawLA, 32 * q, lane);
+          else
+            lora_la_direct<32, F16>(st + L::kLoraLA, p, m_cta, i, 32 * q, lane);
+        }
+        if ((p.lora_tma || p.la16) && p.wcscale != nullptr && !p.prepacked) {
+          const int r0 = L::kBNc / 2 + q * kLuRowsF;
+          if (p.la16)
+            lora_lu_scale<kLuRowsF, 128, F16>(st + L::kLora16LU, st + L::kLoraWC, n_cta, p.N,
+                                              r0, lane, i == 0, lu_inv, zero_col, bad_col);
+          else
+            lora_lu_scale<kLuRowsF, 64, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, r0,
+                                             lane, i == 0, lu_inv, zero_col, bad_col);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        // The pair peer's LoRA rows are generic shared-memory writes that the
+        // leader's MMA reads: the proxy fence above orders them before this
+        // arrival (CTA-scope release, as for every other arrival here).
+        if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
+        // LoRA operands the accumulator cannot carry (this warp's LU' rows),
+        // reported after the arrival
+        warp_report_lora(p.status, kStatusWcscaleZero, zero_col >= 0, zero_col);
+        warp_report_lora(p.status, kStatusLuOverflow, bad_col >= 0, bad_col);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // the K-block items, compiled once per scale layout
+      auto feed_items = [&](auto packed_tag, auto act_tag) {
+        constexpr bool kPacked = decltype(packed_tag)::value;
+        constexpr bool kActPacked = decltype(act_tag)::value;
+        for (int j = 0; ok && j < w.nkb; ++j) {
+          if (!warp_wait_bar<false>(auxfull(stage), phase, kSiteSfAuxFull, ctl)) {
+            ok = false;
+            break;
           }
-          if ((p.lora_tma || p.la16) && p.wcscale != nullptr && !p.prepacked) {
-            const int r0 = L::kBNc / 2 + q * kLuRowsF;
-            if (p.la16)
-              lora_lu_scale<kLuRowsF, 128, F16>(st + L::kLora16LU, st + L::kLoraWC, n_cta, p.N,
-                                                r0, lane, i == 0, lu_inv, zero_col, bad_col);
-            else
-              lora_lu_scale<kLuRowsF, 64, F16>(st + L::kLoraLU, st + L::kLoraWC, n_cta, p.N, r0,
-                                               lane, i == 0, lu_inv, zero_col, bad_col);
-          }
-          ptx::fence_proxy_async_smem();
-        } else {
           const uint8_t* st = smem + stage * L::kStageBytes;
           // Every feeder writes the same words into its own lane quadrant:
           // the block-scaled MMA reads the scale words in every quadrant.
@@ -1254,89 +1282,75 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Packed scales arrive as words [step][rows]: lane a's four words of a
           // 128-row block are 16 consecutive bytes (weights: prepacked;
           // activations: act_scales_packed).
-          auto feed = [&](auto packed_tag, auto act_tag) {
-            constexpr bool kPacked = decltype(packed_tag)::value;
-            constexpr bool kActPacked = decltype(act_tag)::value;
 #pragma unroll
-            for (int kk = 0; kk < KBI; ++kk) {
-              uint32_t a[16], b[16 * L::kSfbHalves];
+          for (int kk = 0; kk < KBI; ++kk) {
+            uint32_t a[16], b[16 * L::kSfbHalves];
 #pragma unroll
-              for (int s4 = 0; s4 < 4; ++s4) {
-                const int ks = 4 * kk + s4;
-                if (kActPacked) {
-                  const uint4 va = lds128(st + L::kOffSFA + 4 * kBM * ks + 16 * lane);
-                  a[4 * s4] = va.x;
-                  a[4 * s4 + 1] = va.y;
-                  a[4 * s4 + 2] = va.z;
-                  a[4 * s4 + 3] = va.w;
-                } else {
-                  sf_words(st + L::kOffSFA + 4 * kBM * ks, kBM, lane, a + 4 * s4);
-                }
-#pragma unroll
-                for (int h = 0; h < L::kSfbHalves; ++h) {
-                  uint32_t* bw = b + 4 * (s4 * L::kSfbHalves + h);
-                  if (kPacked) {
-                    const uint4 v =
-                        lds128(st + L::kOffSFB + 4 * BN * ks + 4 * (128 * h + 4 * lane));
-                    bw[0] = v.x;
-                    bw[1] = v.y;
-                    bw[2] = v.z;
-                    bw[3] = v.w;
-                  } else {
-                    sf_words(st + L::kOffSFB + 4 * BN * ks + 128 * h, BN, lane, bw);
-                  }
-                }
-              }
-              if (KBI == 1 && L::kSfbHalves == 2) {
-                // one K block: SFA (16 columns) and SFB (32) are adjacent; two
-                // stores instead of three (each store briefly holds up the MMAs)
-                uint32_t v[32];
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                  v[x] = a[x];
-                  v[16 + x] = b[x];
-                }
-                ptx::tmem_st_32x32b_x32(col, v);
-                ptx::tmem_st_32x32b_x16(col + 32, b + 16);
+            for (int s4 = 0; s4 < 4; ++s4) {
+              const int ks = 4 * kk + s4;
+              if (kActPacked) {
+                const uint4 va = lds128(st + L::kOffSFA + 4 * kBM * ks + 16 * lane);
+                a[4 * s4] = va.x;
+                a[4 * s4 + 1] = va.y;
+                a[4 * s4 + 2] = va.z;
+                a[4 * s4 + 3] = va.w;
               } else {
-                ptx::tmem_st_32x32b_x16(col + 16 * kk, a);
+                sf_words(st + L::kOffSFA + 4 * kBM * ks, kBM, lane, a + 4 * s4);
+              }
 #pragma unroll
-                for (int h = 0; h < L::kSfbHalves; ++h)
-                  ptx::tmem_st_32x32b_x16(col + 4 * L::kSteps + 16 * L::kSfbHalves * kk + 16 * h,
-                                          b + 16 * h);
+              for (int h = 0; h < L::kSfbHalves; ++h) {
+                uint32_t* bw = b + 4 * (s4 * L::kSfbHalves + h);
+                if (kPacked) {
+                  const uint4 v =
+                      lds128(st + L::kOffSFB + 4 * BN * ks + 4 * (128 * h + 4 * lane));
+                  bw[0] = v.x;
+                  bw[1] = v.y;
+                  bw[2] = v.z;
+                  bw[3] = v.w;
+                } else {
+                  sf_words(st + L::kOffSFB + 4 * BN * ks + 128 * h, BN, lane, bw);
+                }
               }
             }
-          };
-          if (p.prepacked) {
-            if (p.act_packed)
-              feed(std::true_type{}, std::true_type{});
-            else
-              feed(std::true_type{}, std::false_type{});
-          } else if (p.act_packed) {
-            feed(std::false_type{}, std::true_type{});
-          } else {
-            feed(std::false_type{}, std::false_type{});
+            if (KBI == 1 && L::kSfbHalves == 2) {
+              // one K block: SFA (16 columns) and SFB (32) are adjacent; two
+              // stores instead of three (each store briefly holds up the MMAs)
+              uint32_t v[32];
+#pragma unroll
+              for (int x = 0; x < 16; ++x) {
+                v[x] = a[x];
+                v[16 + x] = b[x];
+              }
+              ptx::tmem_st_32x32b_x32(col, v);
+              ptx::tmem_st_32x32b_x16(col + 32, b + 16);
+            } else {
+              ptx::tmem_st_32x32b_x16(col + 16 * kk, a);
+#pragma unroll
+              for (int h = 0; h < L::kSfbHalves; ++h)
+                ptx::tmem_st_32x32b_x16(col + 4 * L::kSteps + 16 * L::kSfbHalves * kk + 16 * h,
+                                        b + 16 * h);
+            }
           }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        __syncwarp();
-        // The pair peer's LoRA rows are generic shared-memory writes that the
-        // leader's MMA reads: the proxy fence above orders them before this
-        // arrival (CTA-scope release, as for every other arrival here).
-        if (lane == 0) ptx::mbar_arrive_remote(full_bar0 + 8u * stage);
-        // LoRA operands the accumulator cannot carry (this warp's LU' rows),
-        // reported after the arrival
-        if (i < w.lora) {
-          warp_report_lora(p.status, kStatusWcscaleZero, zero_col >= 0, zero_col);
-          warp_report_lora(p.status, kStatusLuOverflow, bad_col >= 0, bad_col);
-        }
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      };
+      if (p.prepacked) {
+        if (p.act_packed)
+          feed_items(std::true_type{}, std::true_type{});
+        else
+          feed_items(std::true_type{}, std::false_type{});
+      } else if (p.act_packed) {
+        feed_items(std::false_type{}, std::true_type{});
+      } else {
+        feed_items(std::false_type{}, std::false_type{});
       }
-      if (!ok) break;
     }
   }
 
