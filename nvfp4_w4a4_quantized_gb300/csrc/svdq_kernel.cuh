@@ -828,91 +828,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc_stage * BN);
-        for (int i = 0; i < n_items; ++i, ++j) {
-          if (!wait_bar<CG == 2>(full(stage), phase, kSiteMmaFull, ctl)) {
-            ok = false;
-            break;
-          }
-          if ((j & 1u) == me) {
-            // Everything the MMAs need is computed before this issuer's turn.
-            const uint32_t st = sbase + stage * L::kStageBytes;
-            const bool lora_item = i < w.lora;
-            int nsteps;  // MMAs of this item
-            if (lora_item) {
-              nsteps = min(p.lora_ranks / 16, (p.r16 - p.lora_ranks * i) / 16);
-            } else {
-              // K=64 steps present in this item (the last K block may be partial)
-              nsteps = L::kSteps;
-              if (k_ragged) {
-                const int kb0 = KBI * unit_k_item<SK>(p, w, i - w.lora, rot);
-                nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
-              }
-            }
-            const uint32_t sf = tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
-            // descriptors of this stage's first K step; a step advances the
-            // start address (descriptor units of 16 bytes)
-            const uint64_t soff = static_cast<uint64_t>((stage * L::kStageBytes) >> 4);
-            const uint64_t ad0 = desc_a0 + soff, bd0 = desc_b0 + soff;
-            auto step = [&](int ks) {
-              const int kk = ks >> 2, s4 = ks & 3;
-              const uint64_t ad = ad0 + static_cast<uint64_t>((kk * L::kATile + 32 * s4) >> 4);
-              const uint64_t bd = bd0 + static_cast<uint64_t>((kk * L::kBTile + 32 * s4) >> 4);
-              const uint32_t sfa = sf + 4 * ks;
-              const uint32_t sfb = sf + 4 * L::kSteps + 4 * ks * L::kSfbHalves;
-              if (CG == 2)
-                ptx::mma_mxf4nvf4_pair(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
-              else
-                ptx::mma_mxf4nvf4(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
-            };
-            // Items reach the tensor core in ring order: the fp32 accumulation
-            // order, and with it every output bit, is the same on every call
-            // (unless the caller relaxed the order for the last few percent).
-            // Item j - 1 is the other issuer's ((j - 1) >> 1)-th item, i.e. the
-            // completion of that phase of its turn barrier.
-            if (p.ordered && j > 0 &&
-                !wait_bar<false>(turn(me ^ 1u), ((j - 1u) >> 1) & 1u, kSiteMmaTurn, ctl)) {
+        // LoRA items, then K-block items: one loop each, compiled apart
+        auto run_items = [&](auto lora_tag, int i0, int i1) {
+          constexpr bool kLoraItems = decltype(lora_tag)::value;
+          for (int i = i0; ok && i < i1; ++i, ++j) {
+            if (!wait_bar<CG == 2>(full(stage), phase, kSiteMmaFull, ctl)) {
               ok = false;
               break;
             }
-            ptx::tc_fence_after();
-            if (lora_item) {
-              for (int s = 0; s < nsteps; ++s) {
-                const uint64_t ad = p.la16 ? ptx::desc_kmajor_sw128(st + L::kLora16LA + 32 * s)
-                                           : ptx::desc_kmajor_sw64(st + L::kLoraLA + 32 * s);
-                const uint64_t bd = p.la16 ? ptx::desc_kmajor_sw128(st + L::kLora16LU + 32 * s)
-                                           : ptx::desc_kmajor_sw64(st + L::kLoraLU + 32 * s);
-                if (CG == 2)
-                  ptx::mma_bf16_pair(d_tmem, ad, bd, kIdescLora, 1u);
-                else
-                  ptx::mma_bf16(d_tmem, ad, bd, kIdescLora, 1u);
+            if ((j & 1u) == me) {
+              // Everything the MMAs need is computed before this issuer's turn.
+              const uint32_t st = sbase + stage * L::kStageBytes;
+              int nsteps;  // MMAs of this item
+              if constexpr (kLoraItems) {
+                nsteps = min(p.lora_ranks / 16, (p.r16 - p.lora_ranks * i) / 16);
+              } else {
+                // K=64 steps present in this item (the last K block may be partial)
+                nsteps = L::kSteps;
+                if (k_ragged) {
+                  const int kb0 = KBI * unit_k_item<SK>(p, w, i - w.lora, rot);
+                  nsteps = min(L::kSteps, (p.K - kb0 * kBK) / 64);
+                }
               }
-            } else if (nsteps == L::kSteps) {
+              const uint32_t sf =
+                  tmem_base + static_cast<uint32_t>(L::kAccCols + stage * L::kSfCols);
+              // descriptors of this stage's first K step; a step advances the
+              // start address (descriptor units of 16 bytes)
+              const uint64_t soff = static_cast<uint64_t>((stage * L::kStageBytes) >> 4);
+              const uint64_t ad0 = desc_a0 + soff, bd0 = desc_b0 + soff;
+              auto step = [&](int ks) {
+                const int kk = ks >> 2, s4 = ks & 3;
+                const uint64_t ad = ad0 + static_cast<uint64_t>((kk * L::kATile + 32 * s4) >> 4);
+                const uint64_t bd = bd0 + static_cast<uint64_t>((kk * L::kBTile + 32 * s4) >> 4);
+                const uint32_t sfa = sf + 4 * ks;
+                const uint32_t sfb = sf + 4 * L::kSteps + 4 * ks * L::kSfbHalves;
+                if (CG == 2)
+                  ptx::mma_mxf4nvf4_pair(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
+                else
+                  ptx::mma_mxf4nvf4(d_tmem, ad, bd, kIdescMain, sfa, sfb, 1u);
+              };
+              // Items reach the tensor core in ring order: the fp32 accumulation
+              // order, and with it every output bit, is the same on every call
+              // (unless the caller relaxed the order for the last few percent).
+              // Item j - 1 is the other issuer's ((j - 1) >> 1)-th item, i.e. the
+              // completion of that phase of its turn barrier.
+              if (p.ordered && j > 0 &&
+                  !wait_bar<false>(turn(me ^ 1u), ((j - 1u) >> 1) & 1u, kSiteMmaTurn, ctl)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              if constexpr (kLoraItems) {
+                for (int s = 0; s < nsteps; ++s) {
+                  const uint64_t ad = p.la16 ? ptx::desc_kmajor_sw128(st + L::kLora16LA + 32 * s)
+                                             : ptx::desc_kmajor_sw64(st + L::kLoraLA + 32 * s);
+                  const uint64_t bd = p.la16 ? ptx::desc_kmajor_sw128(st + L::kLora16LU + 32 * s)
+                                             : ptx::desc_kmajor_sw64(st + L::kLoraLU + 32 * s);
+                  if (CG == 2)
+                    ptx::mma_bf16_pair(d_tmem, ad, bd, kIdescLora, 1u);
+                  else
+                    ptx::mma_bf16(d_tmem, ad, bd, kIdescLora, 1u);
+                }
+              } else if (nsteps == L::kSteps) {
 #pragma unroll
-              for (int ks = 0; ks < L::kSteps; ++ks) step(ks);
+                for (int ks = 0; ks < L::kSteps; ++ks) step(ks);
+              } else {
+                for (int ks = 0; ks < nsteps; ++ks) step(ks);
+              }
+              // Hand the turn over (see above).
+              if (p.ordered) {
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(turn(me));
+              }
+              if (CG == 2)
+                ptx::mma_commit_pair_multicast(empty(stage), 3);
+              else
+                ptx::mma_commit(empty(stage));
             } else {
-              for (int ks = 0; ks < nsteps; ++ks) step(ks);
+              // Not this issuer's item: sign the stage's release anyway, so the
+              // producers refill it only after both issuers have passed its
+              // full barrier (neither can then be lapped on that barrier).
+              ptx::mbar_arrive(empty(stage));
+              if (CG == 2) ptx::mbar_arrive_remote(ptx::mapa(empty(stage), 1));
             }
-            // Hand the turn over (see above).
-            if (p.ordered) {
-              ptx::tc_fence_before();
-              ptx::mbar_arrive(turn(me));
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
             }
-            if (CG == 2)
-              ptx::mma_commit_pair_multicast(empty(stage), 3);
-            else
-              ptx::mma_commit(empty(stage));
-          } else {
-            // Not this issuer's item: sign the stage's release anyway, so the
-            // producers refill it only after both issuers have passed its
-            // full barrier (neither can then be lapped on that barrier).
-            ptx::mbar_arrive(empty(stage));
-            if (CG == 2) ptx::mbar_arrive_remote(ptx::mapa(empty(stage), 1));
           }
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+        };
+        run_items(std::true_type{}, 0, w.lora);
+        run_items(std::false_type{}, w.lora, n_items);
         if (!ok) break;
         // this issuer's share of the tile is done (the epilogue waits for both)
         if (CG == 2)
