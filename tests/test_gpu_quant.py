@@ -197,3 +197,53 @@ def test_lora_act_16bit_is_the_rounded_fp32_result(M, K, R, half):
     assert code == 0, (code, site)
     assert la16.dtype == x.dtype
     assert torch.equal(la16, la32.to(x.dtype))
+
+
+def test_layer_in_a_cuda_graph():
+    # x -> svdq_quantize_act (packed scales, 16-bit LoRA activations) ->
+    # svdq_w4a4_gemm_prepacked, captured once in a CUDA graph and replayed on new
+    # x copied into the same buffer: every replay gives the eager calls' bits,
+    # and sampled rows match the oracle's quantiser and operator
+    M, N, K, R = 512, 768, 1024, 32
+    w = synth.make_inputs(M, N, K, R, seed=70)
+    dd = to_device(w)
+    wpk, lup = binding.svdq_prepack_weights(dd["wscales"], dd["lora_up"], dd["wcscale"])
+    ld = synth.make_activations(M, K, R, 71)["lora_down"]
+    xs = [synth.make_activations(M, K, R, 72 + i)["x"] for i in range(3)]
+    x_buf, ld_d = xs[0].cuda(), ld.cuda()
+    act = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    apk = torch.empty((K // 64, M), dtype=torch.int32, device="cuda")
+    la = torch.empty((M, R), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    opts = dict(act_scales_packed=1, lora_act_16bit=1)
+
+    def layer(stream):
+        binding.svdq_quantize_act(x_buf, ld_d, act=act, ascales=apk, lora_act_in=la,
+                                  scales_packed=True, lora_act_16bit=True, stream=stream)
+        binding.svdq_w4a4_gemm_prepacked(act, dd["wgt"], apk, wpk, la, lup, dd["wcscale"],
+                                         dd["bias"], out, stream=stream, options=opts)
+
+    layer(torch.cuda.current_stream())  # the library's one-time set-up, outside the capture
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        layer(torch.cuda.current_stream())
+    for i, x in enumerate(xs):
+        x_buf.copy_(x)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        code, site, _ = binding.svdq_read_device_status(clear=True)
+        assert code == 0, f"device status {code} at wait site {site} (input {i})"
+        y_graph = out.clone()
+        out.fill_(float("nan"))
+        layer(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert torch.equal(y_graph, out), f"graph replay {i} differs from the eager calls"
+        ref_act, ref_asc = q.quantize_act(x, M, K)
+        ref_la = q.lora_down(x, ld, M, K, R)
+        inp = dict(w, act=torch.from_numpy(ref_act), ascales=torch.from_numpy(ref_asc),
+                   lora_act_in=torch.from_numpy(ref_la).to(torch.bfloat16).to(torch.float32))
+        rows = np.array(sorted({0, 127, 128, 255, 256, 511} | set(range(5, M, 37))))
+        parity(y_graph.double().cpu().numpy()[rows], oracle_y(inp, M, N, K, R, rows=rows))
