@@ -42,9 +42,10 @@
 //                block_scale.scale_vec::4X for main items, kind::f16 (bf16 or
 //                fp16) for LoRA items, commits that free ring stages / publish
 //                accumulators.
-//   warps 2, 3   LoRA operand builders: LU' = round16(LU / wc), half the rows
-//                each, in place in the stage's K-major 64-byte-swizzle layout
-//                (nothing to do for prepacked weights, whose LU' arrives ready).
+//   warps 2, 3   LoRA operand builders: LU' = round16(LU / wc), a quarter of
+//                the rows each (the scale feeders take the other half), in place
+//                in the stage's K-major swizzled layout (nothing to do for
+//                prepacked weights, whose LU' arrives ready).
 //   warps 4..7, 15..18  epilogue, two warps per 32-lane quadrant, each taking
 //                half of the tile's 32-column groups: tcgen05.ld -> fma(acc,
 //                wc, bias) -> 16-bit -> shared staging (64-byte swizzle) -> one
@@ -57,7 +58,11 @@
 //                activation scales handed over packed) and write
 //                them into tensor memory with tcgen05.st (one warp per 32-lane
 //                quadrant), off the MMA pipe; on LoRA items they build
-//                LA' = round16(LA), 32 rows each.
+//                LA' = round16(LA), 32 rows each, and scale their share of LU'.
+// The MMA issuers, the LoRA builders and the scale feeders run a unit's LoRA
+// items and its K-block items in two loops, the feeders' K-block loop once per
+// scale layout: a per-item branch on the item kind or the layout cost 6-20 %
+// through the register allocation of the loop.
 // Warp w accesses tensor-memory lanes 32(w%4) .. 32(w%4)+31, so epilogue warps
 // 4..7 and 15..18 and scale feeders 8..11 each cover all four quadrants.
 //
