@@ -49,7 +49,7 @@ def test_tiny_workload_full_matrix(cfg):
 @pytest.mark.parametrize("M,N,K,R", [
     (272, 144, 320, 20),     # ragged M, N and a partial last K block; R not a multiple of 16
     (16, 16, 64, 1),         # smallest legal shape
-    (400, 528, 1088, 100),   # several tiles, ragged everywhere, two LoRA blocks
+    (400, 528, 1088, 100),   # several tiles, ragged everywhere, four 32-rank LoRA items
     (128, 256, 256, 0),      # no LoRA
     (384, 512, 768, 64),     # exact multiples, one full LoRA block
     (256, 272, 512, 128),    # maximum rank
