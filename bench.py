@@ -40,8 +40,8 @@ packed-scale route and that route with 16-bit LoRA activations, and the
 24-case token-count sweep (default route, plus
 the split-K entry point where the planner splits); then the activation
 quantiser on the production activations (GB/s against the measured HBM copy
-bandwidth) and the whole layer from 16-bit activations (quantiser with
-packed scales + prepacked operator in one event pair).  The headline `value` is
+bandwidth) and the whole layer from 16-bit activations (svdq_w4a4_linear:
+quantiser with packed scales + prepacked operator, in one event pair).  The headline `value` is
 the attention projection, the configuration the metric is quoted on.
 `--no-per-shape` skips that section.
 """
@@ -455,22 +455,20 @@ def run_quantize_shapes(pkg, synth, torch, dev, stream, flush, fp4_peak):
         a = synth.make_activations(w.M, w.K, w.R, seed=w.seed + 100)
         x, ld = a["x"].to(dev), a["lora_down"].to(dev)
         wpk, lup = pkg.svdq_prepack_weights(d["wscales"], d["lora_up"], d["wcscale"])
-        act, apk, la = pkg.svdq_quantize_act(x, ld, scales_packed=True, lora_act_16bit=True)
+        ws = torch.empty(pkg.svdq_linear_workspace_size(w.M, w.K, w.R), dtype=torch.uint8,
+                         device=dev)
         out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
-        o2 = dict(act_scales_packed=1, lora_act_16bit=1)
 
         def call_layer():
-            pkg.svdq_quantize_act(x, ld, act, apk, la, scales_packed=True, lora_act_16bit=True,
-                                  stream=stream)
-            pkg.svdq_w4a4_gemm_prepacked(act, d["wgt"], apk, wpk, la, lup, d["wcscale"],
-                                         d["bias"], out, stream=stream, options=o2)
+            pkg.svdq_w4a4_linear(x, ld, d["wgt"], wpk, lup, d["wcscale"], d["bias"], out,
+                                 workspace=ws, stream=stream)
         e = shape_entry(float(w.flops), time_flushed(call_layer, flush, stream, 3, 10, torch,
                                                      dev), fp4_peak)
-        e["how"] = ("svdq_quantize_act (packed scales, 16-bit LA) + svdq_w4a4_gemm_prepacked "
-                    "(act_scales_packed, lora_act_16bit) in one event pair; tflops counts the "
-                    "operator's 2MNK + 2MNR")
+        e["how"] = ("svdq_w4a4_linear: svdq_quantize_act (packed scales, 16-bit LA) + "
+                    "svdq_w4a4_gemm_prepacked (act_scales_packed, lora_act_16bit), one event "
+                    "pair; tflops counts the operator's 2MNK + 2MNR")
         layer[w.name] = e
-        del d, x, ld, wpk, lup, act, apk, la, out
+        del d, x, ld, wpk, lup, ws, out
     return {"quantize": quant, "layer_from_16bit_x": layer}
 
 

@@ -265,6 +265,43 @@ int svdq_quantize_query(int64_t M, int64_t K, int64_t R, int32_t sm_count, int32
                         int32_t* grid, int32_t* stages, int32_t* smem_bytes);
 
 /*
+ * svdq_w4a4_linear -- the whole layer from 16-bit activations ("SVDQuant W4A4
+ * on Blackwell" §1: the activation quantiser feeding the W4A4 operator of §2):
+ *
+ *     y = scaled_mma(quant(x), wgt4) * wcscale + bias + (x @ lora_down^T) @ lora_up
+ *
+ * as svdq_quantize_act (packed activation scales; the LoRA-down product in x's
+ * 16-bit type when R is a multiple of 8, else in fp32) followed by
+ * svdq_w4a4_gemm_prepacked with act_scales_packed (and lora_act_16bit when the
+ * product is 16-bit), both on `stream`; act, the scale words and lora_act_in
+ * live in `workspace` between the two launches.  The result is that of those
+ * two calls, bit for bit.
+ *
+ * x, lora_down   as for svdq_quantize_act; their 16-bit type is options->io_dtype.
+ * wgt, wscales_packed, lora_up_packed, wcscale, bias, out
+ *                as for svdq_w4a4_gemm_prepacked (weights from svdq_prepack_weights).
+ * M, N, K, R     as for svdq_w4a4_gemm.
+ * options        as for svdq_w4a4_gemm_ex (NULL: defaults); act_scales_packed and
+ *                lora_act_16bit are set by this call.
+ * workspace      device, 256-byte aligned, at least svdq_linear_workspace_size(M, K, R)
+ *                bytes (NULL when that is 0); SVDQ_ERR_WORKSPACE otherwise.
+ *
+ * Returns the first non-OK status of the two steps; if the operator step
+ * rejects its arguments, the quantiser may already be in the stream (it
+ * writes only the workspace).  Asynchronous, allocates nothing.
+ */
+int svdq_w4a4_linear(const void* x, const void* lora_down, const void* wgt,
+                     const void* wscales_packed, const void* lora_up_packed, const void* wcscale,
+                     const void* bias, void* out, int64_t M, int64_t N, int64_t K, int64_t R,
+                     const svdq_options_t* options, void* workspace, int64_t workspace_bytes,
+                     void* stream);
+
+/* Workspace bytes svdq_w4a4_linear needs (host only): act, the packed
+ * activation scales and lora_act_in, each padded to 256 bytes; a negative
+ * status for arguments svdq_w4a4_linear would reject by shape. */
+int64_t svdq_linear_workspace_size(int64_t M, int64_t K, int64_t R);
+
+/*
  * svdq_w4a4_gemm_prepacked -- svdq_w4a4_gemm_ex on prepacked weights: the
  * same operator and result, with wscales_packed and lora_up_packed from
  * svdq_prepack_weights in place of wscales and lora_up.  wcscale must be the
@@ -422,7 +459,7 @@ const char* svdq_status_string(int status);
 /* Library ABI version (major * 10000 + minor * 100 + patch).  The structs
  * above grow only at their end; a caller built against a header with another
  * major.minor (SVDQ_ABI_VERSION / 100) must not pass them to this library. */
-#define SVDQ_ABI_VERSION 700
+#define SVDQ_ABI_VERSION 701
 int svdq_version(void);
 
 #ifdef __cplusplus

@@ -13,4 +13,5 @@ from .binding import (SVDQ_ERR_BAD_OPTION, SVDQ_ERR_INVALID_ARG, SVDQ_ERR_MISALI
                       SVDQ_OK, SvdqError, SvdqOptions, load, status_string, svdq_lora_stage_bytes,
                       svdq_pack_scales, svdq_prepack_weights, svdq_query_plan, svdq_read_device_status,
                       svdq_quantize_act, svdq_quantize_query, svdq_version, svdq_w4a4_gemm,
-                      svdq_w4a4_gemm_prepacked, svdq_w4a4_gemm_split, svdq_workspace_size)
+                      svdq_w4a4_gemm_prepacked, svdq_w4a4_gemm_split, svdq_w4a4_linear,
+                      svdq_linear_workspace_size, svdq_workspace_size)

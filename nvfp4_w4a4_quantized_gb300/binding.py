@@ -15,7 +15,7 @@ from typing import Optional
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsvdq.so")
 # include/svdq.h SVDQ_ABI_VERSION the structs below mirror
-ABI_VERSION = 700
+ABI_VERSION = 701
 # include/svdq.h size limits
 SVDQ_MAX_MN = 1 << 24
 SVDQ_MAX_K = 1 << 20
@@ -44,7 +44,8 @@ EXPORTED = ("svdq_w4a4_gemm", "svdq_w4a4_gemm_ex", "svdq_prepack_weights", "svdq
             "svdq_w4a4_gemm_prepacked", "svdq_w4a4_gemm_split", "svdq_w4a4_gemm_split_noalloc",
             "svdq_workspace_size",
             "svdq_query_plan", "svdq_lora_stage_bytes", "svdq_read_device_status",
-            "svdq_status_string", "svdq_version", "svdq_quantize_act", "svdq_quantize_query")
+            "svdq_status_string", "svdq_version", "svdq_quantize_act", "svdq_quantize_query",
+            "svdq_w4a4_linear", "svdq_linear_workspace_size")
 
 
 class SvdqOptions(ctypes.Structure):
@@ -133,6 +134,11 @@ def load(path: Optional[str] = None):
         lib.svdq_quantize_act.argtypes = [vp, vp] + [i64] * 3 + [i32] * 3 + [vp] * 4
         lib.svdq_quantize_query.restype = ctypes.c_int
         lib.svdq_quantize_query.argtypes = [i64] * 3 + [i32] + [ctypes.POINTER(i32)] * 4
+        lib.svdq_w4a4_linear.restype = ctypes.c_int
+        lib.svdq_w4a4_linear.argtypes = [vp] * 8 + [i64] * 4 + [ctypes.POINTER(SvdqOptions), vp,
+                                                               i64, vp]
+        lib.svdq_linear_workspace_size.restype = i64
+        lib.svdq_linear_workspace_size.argtypes = [i64] * 3
         # the ctypes structs here mirror include/svdq.h at ABI_VERSION
         if lib.svdq_version() // 100 != ABI_VERSION // 100:
             raise RuntimeError(f"{p} has ABI version {lib.svdq_version()}, this binding "
@@ -442,3 +448,58 @@ def svdq_quantize_query(M: int, K: int, R: int, sm_count: int = 0) -> dict:
     if rc != SVDQ_OK:
         raise SvdqError(rc, "svdq_quantize_query")
     return dict(zip(("splits", "grid", "stages", "smem_bytes"), (int(t.value) for t in v)))
+
+
+def svdq_linear_workspace_size(M: int, K: int, R: int) -> int:
+    """Workspace bytes svdq_w4a4_linear needs for x [M, K] and rank R."""
+    n = int(load().svdq_linear_workspace_size(M, K, R))
+    if n < 0:
+        raise SvdqError(n, "svdq_linear_workspace_size")
+    return n
+
+
+def svdq_w4a4_linear(x, lora_down, wgt, wscales_packed, lora_up_packed, wcscale, bias, out,
+                     workspace=None, stream=None, options=None, check: bool = True) -> int:
+    """The whole layer from 16-bit activations x [M, K] (bf16 or fp16):
+    svdq_quantize_act (packed scales, 16-bit LoRA-down product when R % 8 == 0)
+    then svdq_w4a4_gemm_prepacked, into ``out`` [M, N] of x's type.
+    lora_down [R, K] in x's type or None; wgt uint8 [N, K/2]; wscales_packed /
+    lora_up_packed from svdq_prepack_weights; ``workspace`` a uint8 CUDA tensor
+    of at least svdq_linear_workspace_size bytes (allocated here if None)."""
+    import torch
+
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("x must be bf16 or fp16")
+    _check("x", x, x.dtype)
+    _check("out", out, x.dtype)
+    M, K = x.shape
+    N = int(out.shape[1])
+    R = 0 if lora_down is None else int(lora_down.shape[0])
+    if R:
+        _check("lora_down", lora_down, x.dtype)
+        if tuple(lora_down.shape) != (R, K):
+            raise ValueError("lora_down must be [R, K]")
+    _check("wgt", wgt, torch.uint8)
+    _check("wscales_packed", wscales_packed, torch.int32)
+    for name, t in (("lora_up_packed", lora_up_packed if R else None), ("wcscale", wcscale),
+                    ("bias", bias)):
+        if t is not None:
+            _check(name, t, x.dtype)
+    if tuple(wgt.shape) != (N, K // 2) or tuple(out.shape) != (M, N):
+        raise ValueError("inconsistent shapes")
+    need = svdq_linear_workspace_size(M, K, R)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    _check("workspace", workspace, torch.uint8)
+    o = _opts(options)
+    o = SvdqOptions() if o is None else SvdqOptions.from_buffer_copy(o)
+    o.io_dtype = SVDQ_IO_FP16 if x.dtype == torch.float16 else SVDQ_IO_BF16
+    h = _stream_handle(stream, x.device)
+    with torch.cuda.device(x.device):
+        rc = load().svdq_w4a4_linear(_ptr(x), _ptr(lora_down) if R else None, _ptr(wgt),
+                                     _ptr(wscales_packed), _ptr(lora_up_packed) if R else None,
+                                     _ptr(wcscale), _ptr(bias), _ptr(out), M, N, K, R,
+                                     ctypes.byref(o), _ptr(workspace), workspace.numel(), h)
+    if check and rc != SVDQ_OK:
+        raise SvdqError(rc, "svdq_w4a4_linear")
+    return rc

@@ -1086,3 +1086,43 @@ extern "C" int svdq_quantize_query(int64_t M, int64_t K, int64_t R, int32_t sm_c
   if (smem_bytes) *smem_bytes = qp.smem;
   return SVDQ_OK;
 }
+
+extern "C" int64_t svdq_linear_workspace_size(int64_t M, int64_t K, int64_t R) {
+  using namespace svdq;
+  if (M < 0 || K <= 0 || R < 0) return SVDQ_ERR_INVALID_ARG;
+  if (M % 16 || K % 64 || M > SVDQ_MAX_MN || K > SVDQ_MAX_K || R > SVDQ_MAX_RANK)
+    return SVDQ_ERR_UNSUPPORTED_SHAPE;
+  auto pad = [](int64_t b) { return (b + 255) / 256 * 256; };
+  const int64_t la_bytes = R == 0 ? 0 : M * R * (R % 8 == 0 ? 2 : 4);
+  return pad(M * K / 2) + pad(M * K / 16) + pad(la_bytes);
+}
+
+extern "C" int svdq_w4a4_linear(const void* x, const void* lora_down, const void* wgt,
+                                const void* wscales_packed, const void* lora_up_packed,
+                                const void* wcscale, const void* bias, void* out, int64_t M,
+                                int64_t N, int64_t K, int64_t R, const svdq_options_t* options,
+                                void* workspace, int64_t workspace_bytes, void* stream) {
+  using namespace svdq;
+  const int64_t need = svdq_linear_workspace_size(M, K, R);
+  if (need < 0) return static_cast<int>(need);
+  if (N < 0) return SVDQ_ERR_INVALID_ARG;
+  if (N % 16 || N > SVDQ_MAX_MN) return SVDQ_ERR_UNSUPPORTED_SHAPE;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
+    return SVDQ_ERR_WORKSPACE;
+  svdq_options_t o{};
+  if (options != nullptr) o = *options;
+  const int32_t la16 = (R > 0 && R % 8 == 0) ? 1 : 0;
+  o.act_scales_packed = 1;
+  o.lora_act_16bit = la16;
+  // act [M][K/2], scale words [K/64][M], lora_act_in [M][R], each 256-byte aligned
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t off_sc = (M * K / 2 + 255) / 256 * 256;
+  const int64_t off_la = off_sc + (M * K / 16 + 255) / 256 * 256;
+  void* act = ws;
+  void* asc = ws != nullptr ? ws + off_sc : nullptr;
+  void* la = (ws != nullptr && R > 0) ? ws + off_la : nullptr;
+  int rc = svdq_quantize_act(x, lora_down, M, K, R, o.io_dtype, 1, la16, act, asc, la, stream);
+  if (rc != SVDQ_OK) return rc;
+  return svdq_w4a4_gemm_prepacked(act, wgt, asc, wscales_packed, static_cast<const float*>(la),
+                                  lora_up_packed, wcscale, bias, out, M, N, K, R, &o, stream);
+}

@@ -350,3 +350,36 @@ def test_quantize_plan(lib, M, K, R, splits):
     assert plan["stages"] * stage >= 128 * (r16 + 4) * 4
     assert plan["smem_bytes"] >= plan["stages"] * stage
     assert plan["smem_bytes"] <= 232448
+
+
+@pytest.mark.parametrize("M,K,R", [(0, 64, 0), (16, 64, 0), (4096, 3072, 32), (4096, 12288, 128),
+                                   (272, 640, 20), (16, 128, 8)])
+def test_linear_workspace_size(lib, M, K, R):
+    # act [M][K/2], scale words [K/64][M], lora_act_in [M][R] (16-bit when R % 8 == 0,
+    # else fp32), each padded to 256 bytes
+    pad = lambda b: -(-b // 256) * 256
+    la = 0 if R == 0 else M * R * (2 if R % 8 == 0 else 4)
+    assert binding.svdq_linear_workspace_size(M, K, R) == pad(M * K // 2) + pad(M * K // 16) + pad(la)
+
+
+@pytest.mark.parametrize("M,K,R,expect", [(-16, 64, 0, binding.SVDQ_ERR_INVALID_ARG),
+                                          (16, 0, 0, binding.SVDQ_ERR_INVALID_ARG),
+                                          (24, 64, 0, binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+                                          (16, 96, 0, binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+                                          (16, 64, 129, binding.SVDQ_ERR_UNSUPPORTED_SHAPE)])
+def test_linear_workspace_size_rejects(lib, M, K, R, expect):
+    assert lib.svdq_linear_workspace_size(M, K, R) == expect
+
+
+@pytest.mark.parametrize("N,ws_off,ws_bytes,expect", [
+    (64, 0, 1024, binding.SVDQ_ERR_WORKSPACE),    # too small
+    (64, 16, 1 << 20, binding.SVDQ_ERR_WORKSPACE),  # not 256-byte aligned
+    (72, 0, 1 << 20, binding.SVDQ_ERR_UNSUPPORTED_SHAPE),
+    (-16, 0, 1 << 20, binding.SVDQ_ERR_INVALID_ARG),
+])
+def test_linear_host_validation(lib, N, ws_off, ws_bytes, expect):
+    # rejected before any device call (the addresses are fake)
+    M, K, R = 32, 128, 0
+    rc = lib.svdq_w4a4_linear(A, None, A, A, None, None, None, A, M, N, K, R, None, A + ws_off,
+                              ws_bytes, None)
+    assert rc == expect

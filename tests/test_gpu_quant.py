@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import oracle_y, parity, to_device
+from gpu_util import oracle_y, parity, sample_rows, to_device
 from nvfp4_w4a4_quantized_gb300 import binding, synth
 from oracle import quant_ref as q
 
@@ -247,3 +247,58 @@ def test_layer_in_a_cuda_graph():
                    lora_act_in=torch.from_numpy(ref_la).to(torch.bfloat16).to(torch.float32))
         rows = np.array(sorted({0, 127, 128, 255, 256, 511} | set(range(5, M, 37))))
         parity(y_graph.double().cpu().numpy()[rows], oracle_y(inp, M, N, K, R, rows=rows))
+
+
+@pytest.mark.parametrize("half", [False, True], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("M,N,K,R", [(272, 400, 640, 0), (272, 400, 640, 20), (512, 768, 1024, 32),
+                                     (384, 512, 3072, 128)])
+def test_linear_is_the_two_calls(M, N, K, R, half):
+    # svdq_w4a4_linear (one call from 16-bit x) gives the bits of svdq_quantize_act
+    # + svdq_w4a4_gemm_prepacked, and sampled rows match the oracle's quantiser
+    # and operator
+    h16 = torch.float16 if half else torch.bfloat16
+    w = synth.make_inputs(M, N, K, R, seed=80 + R, half=half)
+    a = synth.make_activations(M, K, R, 81 + R, half=half)
+    dd = to_device(w)
+    wpk, lup = binding.svdq_prepack_weights(dd["wscales"], dd["lora_up"] if R else None,
+                                            dd["wcscale"])
+    x, ld = a["x"].cuda(), (a["lora_down"].cuda() if R else None)
+    out = torch.full((M, N), float("nan"), dtype=h16, device="cuda")
+    binding.svdq_w4a4_linear(x, ld, dd["wgt"], wpk, lup if R else None, dd["wcscale"], dd["bias"],
+                             out)
+    la16 = R > 0 and R % 8 == 0
+    act, apk, la = binding.svdq_quantize_act(x, ld, scales_packed=True, lora_act_16bit=la16)
+    ref = torch.full((M, N), float("nan"), dtype=h16, device="cuda")
+    binding.svdq_w4a4_gemm_prepacked(act, dd["wgt"], apk, wpk, la, lup if R else None,
+                                     dd["wcscale"], dd["bias"], ref,
+                                     options=dict(act_scales_packed=1, lora_act_16bit=int(la16),
+                                                  io_dtype=int(half)))
+    torch.cuda.synchronize()
+    code, site, _ = binding.svdq_read_device_status(clear=True)
+    assert code == 0, (code, site)
+    assert torch.equal(out, ref)
+    ref_act, ref_asc = q.quantize_act(a["x"], M, K, half=half)
+    inp = dict(w, act=torch.from_numpy(ref_act), ascales=torch.from_numpy(ref_asc))
+    if R:
+        ref_la = torch.from_numpy(q.lora_down(a["x"], a["lora_down"], M, K, R, half))
+        inp["lora_act_in"] = (ref_la.to(h16) if la16 else ref_la).to(torch.float32)
+    else:
+        inp["lora_act_in"] = None
+        inp["lora_up"] = None
+    rows = sample_rows(M, 24, seed=R)
+    parity(out.double().cpu().numpy()[rows], oracle_y(inp, M, N, K, R, rows=rows))
+
+
+def test_linear_rejects_a_small_workspace():
+    M, N, K, R = 256, 256, 256, 32
+    x = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    wgt = torch.zeros(N, K // 2, dtype=torch.uint8, device="cuda")
+    wpk = torch.zeros(K // 64, N, dtype=torch.int32, device="cuda")
+    lup = torch.zeros(N, R, dtype=torch.bfloat16, device="cuda")
+    ld = torch.zeros(R, K, dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(binding.svdq_linear_workspace_size(M, K, R) - 256, dtype=torch.uint8,
+                     device="cuda")
+    rc = binding.svdq_w4a4_linear(x, ld, wgt, wpk, lup, None, None, out, workspace=ws,
+                                  check=False)
+    assert rc == binding.SVDQ_ERR_WORKSPACE
