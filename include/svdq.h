@@ -375,8 +375,8 @@ int svdq_w4a4_gemm_split(const void* act, const void* wgt, const void* ascales,
  * Arguments are those of svdq_w4a4_gemm_split without the workspace.  Plans
  * needing more than SVDQ_NOALLOC_SCRATCH_BYTES (svdq_workspace_size) return
  * SVDQ_ERR_SCRATCH_LIMIT before anything is launched.  The first call on a
- * device looks up the array's device address (a one-time set-up per device);
- * make that first call before any stream capture.  Every call on a device
+ * device looks up the array's device address (one cudaGetSymbolAddress per
+ * device, under the library's lock).  Every call on a device
  * shares the one array: calls that overlap on the GPU (other streams, other
  * threads) race on it and must be serialised by the caller.  The array
  * starts zero-filled and every completed call leaves its flags at zero, so
