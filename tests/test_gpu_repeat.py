@@ -101,3 +101,65 @@ def test_relaxed_order_routes_within_bound(route, cfg):
     ref = oracle_y(inp, M, N, K, R)
     for _ in range(2):
         parity(ROUTES[route](inp, M, N, K, R, dict(cfg, relaxed_order=1)), ref)
+
+
+def test_concurrent_calls_from_two_threads_on_two_streams():
+    # the library is thread-safe and calls on different streams are independent:
+    # two host threads, each on its own stream, issue the operator and the
+    # activation quantiser on different shapes (different plans, tensor maps and
+    # one-time set-up) at once; every output equals the serial call's bits
+    import threading
+
+    from gpu_util import to_device
+
+    shapes = [(512, 768, 1024, 32), (384, 512, 2048, 128)]
+    devs = [to_device(synth.make_inputs(*s, seed=90 + i)) for i, s in enumerate(shapes)]
+    xs = [synth.make_activations(M, K, R, seed=95 + i) for i, (M, N, K, R) in enumerate(shapes)]
+    xs = [(a["x"].cuda(), a["lora_down"].cuda()) for a in xs]
+
+    def gemm(i, out, stream=None):
+        d = devs[i]
+        binding.svdq_w4a4_gemm(d["act"], d["wgt"], d["ascales"], d["wscales"], d["lora_act_in"],
+                               d["lora_up"], d["wcscale"], d["bias"], out, stream=stream)
+
+    def quant(i, stream=None):
+        return binding.svdq_quantize_act(*xs[i], stream=stream)
+
+    refs = []
+    for i, (M, N, K, R) in enumerate(shapes):
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        gemm(i, out)
+        refs.append((out, quant(i)))
+    torch.cuda.synchronize()
+    results, errors = [None, None], []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            M, N, K, R = shapes[i]
+            got = []
+            with torch.cuda.stream(s):
+                for _ in range(8):
+                    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+                    gemm(i, out, stream=s)
+                    got.append((out, quant(i, stream=s)))
+            s.synchronize()
+            results[i] = got
+        except Exception as e:  # re-raised in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    code, site, _ = binding.svdq_read_device_status(clear=True)
+    assert code == 0, (code, site)
+    for i in range(2):
+        ref_out, ref_q = refs[i]
+        for out, qo in results[i]:
+            assert torch.equal(out, ref_out)
+            for a, b in zip(qo, ref_q):
+                assert torch.equal(a, b)
