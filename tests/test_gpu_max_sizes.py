@@ -1,6 +1,7 @@
-"""The operator at the header's size limits (SVDQ_MAX_K = 2^20, SVDQ_MAX_MN =
-2^24), through the C ABI: index arithmetic (tile and row coordinates, byte
-offsets of operands, scales, LoRA rows and the output) must not overflow.
+"""The operator and the activation quantiser at the header's size limits
+(SVDQ_MAX_K = 2^20, SVDQ_MAX_MN = 2^24), through the C ABI: index arithmetic
+(tile and row coordinates, byte offsets of operands, scales, LoRA rows and the
+outputs) must not overflow.
 
 The operator is separable: output rows depend only on their act / ascales /
 lora_act_in rows, output columns only on their wgt / wscales / lora_up /
@@ -61,3 +62,36 @@ def test_max_n():
                lora_up=inp["lora_up"][cols].contiguous(), wcscale=inp["wcscale"][cols].contiguous(),
                bias=inp["bias"][cols].contiguous())
     parity(y[:, cols], oracle_y(sub, M, len(cols), K, R))
+
+
+def _quant_check(x, ld, M, K, R, rows):
+    # the quantiser is separable by rows: codes, scales and LoRA-down of the
+    # sampled rows against the oracle on those rows alone
+    from oracle import quant_ref as q
+
+    act, asc, la = binding.svdq_quantize_act(x.cuda(), ld.cuda() if R else None)
+    torch.cuda.synchronize()
+    code, site, _ = binding.svdq_read_device_status(clear=True)
+    assert code == 0, (code, site)
+    idx = torch.tensor(rows)
+    xr = x[idx]
+    want_act, want_asc = q.quantize_act(xr, len(rows), K)
+    np.testing.assert_array_equal(act[idx.cuda()].cpu().numpy(), want_act)
+    np.testing.assert_array_equal(asc[:, idx.cuda()].cpu().numpy(), want_asc)
+    if R:
+        ref = q.lora_down(xr, ld, len(rows), K, R)
+        mag = np.abs(q.decode_x(xr, len(rows), K)) @ np.abs(q.decode_x(ld, R, K)).T
+        err = np.abs(la[idx.cuda()].double().cpu().numpy() - ref)
+        assert np.all(err <= K * 2.0 ** -22 * mag + 1e-30)
+
+
+def test_quantiser_max_k():
+    M, K, R = 16, binding.SVDQ_MAX_K, 32
+    a = synth.make_activations(M, K, R, seed=24)
+    _quant_check(a["x"], a["lora_down"], M, K, R, list(range(M)))
+
+
+def test_quantiser_max_m():
+    M, K, R = binding.SVDQ_MAX_MN, 64, 8
+    a = synth.make_activations(M, K, R, seed=25)
+    _quant_check(a["x"], a["lora_down"], M, K, R, _edges(M, 40, 4))
