@@ -302,3 +302,41 @@ def test_linear_rejects_a_small_workspace():
     rc = binding.svdq_w4a4_linear(x, ld, wgt, wpk, lup, None, None, out, workspace=ws,
                                   check=False)
     assert rc == binding.SVDQ_ERR_WORKSPACE
+
+
+def test_linear_in_a_cuda_graph():
+    # one svdq_w4a4_linear call captured in a CUDA graph and replayed on new x
+    # copied into the same buffer: each replay gives the eager call's bits
+    M, N, K, R = 512, 768, 1024, 40
+    w = synth.make_inputs(M, N, K, R, seed=74)
+    dd = to_device(w)
+    wpk, lup = binding.svdq_prepack_weights(dd["wscales"], dd["lora_up"], dd["wcscale"])
+    ld = synth.make_activations(M, K, R, 75)["lora_down"].cuda()
+    xs = [synth.make_activations(M, K, R, 76 + i)["x"] for i in range(3)]
+    x_buf = xs[0].cuda()
+    ws = torch.empty(binding.svdq_linear_workspace_size(M, K, R), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+
+    def layer(stream):
+        binding.svdq_w4a4_linear(x_buf, ld, dd["wgt"], wpk, lup, dd["wcscale"], dd["bias"], out,
+                                 workspace=ws, stream=stream)
+
+    layer(torch.cuda.current_stream())  # the library's one-time set-up, outside the capture
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        layer(torch.cuda.current_stream())
+    for i, x in enumerate(xs):
+        x_buf.copy_(x)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        code, site, _ = binding.svdq_read_device_status(clear=True)
+        assert code == 0, (code, site, i)
+        y_graph = out.clone()
+        out.fill_(float("nan"))
+        layer(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert torch.equal(y_graph, out), f"graph replay {i} differs from the eager call"
